@@ -1,0 +1,212 @@
+"""Seeded synthetic inputs for the CSA fused Compressor.
+
+This module only draws inputs: segment lengths, packed ``cu_seqlens`` /
+``cu_seqlens_comp`` offsets and the random kv / score / ape / grad_out tensors.
+It holds none of the Compressor's arithmetic, so the CPU oracle and the CUDA
+library can both be fed from it without sharing any of the method.
+
+Random numbers come from SplitMix64 (Steele, Lea and Flood, "Fast splittable
+pseudorandom number generators", OOPSLA 2014) run as a counter-based generator
+(value i of stream ``seed`` is the SplitMix64 finaliser of ``seed*GOLDEN +
+(i+1)*GOLDEN``), turned into normals with the Box-Muller transform and rounded
+to bf16 with round-to-nearest-even.  Everything is numpy, so the same seed
+gives the same bits on x86_64 and aarch64.
+
+Distributions follow the Numerics section of the "CSA Fused Compressor" page
+(cuDNN frontend docs): kv, grad_out ~ N(0, 1) bf16, score ~ N(0, 1.5^2) bf16,
+ape ~ N(0, 0.25^2) fp32.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# Per-tensor stream ids, so that each tensor of a case has its own stream.
+STREAM_KV = 1
+STREAM_SCORE = 2
+STREAM_APE = 3
+STREAM_GRAD = 4
+STREAM_LENGTHS = 5
+
+
+def splitmix64(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
+    """n uint64 values of the counter-based SplitMix64 stream (seed, stream)."""
+    key = np.uint64((seed * 0x100000001B3 + stream * 0x9E3779B1) & 0xFFFFFFFFFFFFFFFF)
+    with np.errstate(over="ignore"):
+        ctr = np.arange(offset + 1, offset + n + 1, dtype=np.uint64)
+        z = key * _GOLDEN + ctr * _GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def uniform01(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
+    """n doubles in (0, 1): the top 53 bits of each draw, shifted off zero."""
+    z = splitmix64(seed, stream, n, offset)
+    return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
+
+
+def normal(seed: int, stream: int, n: int, sigma: float = 1.0) -> np.ndarray:
+    """n N(0, sigma^2) doubles by Box-Muller (two uniforms per pair)."""
+    m = (n + 1) // 2
+    u = uniform01(seed, stream, 2 * m)
+    u1, u2 = u[0::2], u[1::2]
+    rad = np.sqrt(-2.0 * np.log(u1))
+    ang = 2.0 * np.pi * u2
+    z = np.empty(2 * m, dtype=np.float64)
+    z[0::2] = rad * np.cos(ang)
+    z[1::2] = rad * np.sin(ang)
+    return z[:n] * sigma
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    nan = (u & 0x7FFFFFFF) > 0x7F800000
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    r[nan] = 0x7FC0
+    return r
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float32 values (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+@dataclasses.dataclass
+class Case:
+    """One Compressor problem: THD offsets plus the random tensors (host numpy)."""
+    name: str
+    ratio: int
+    coff: int
+    head_dim: int
+    seqlens: list
+    capacity: int
+    n_tokens: int
+    cu_seqlens: np.ndarray       # int32 [n_seg+1]
+    cu_seqlens_comp: np.ndarray  # int32 [n_seg+1]
+    kv: np.ndarray               # uint16 (bf16 bits) [n_tokens, coff*head_dim]
+    score: np.ndarray            # uint16 (bf16 bits) [n_tokens, coff*head_dim]
+    ape: np.ndarray              # float32 [ratio, coff*head_dim]
+    grad_out: np.ndarray         # uint16 (bf16 bits) [capacity, head_dim]
+
+    @property
+    def n_seg(self) -> int:
+        return len(self.seqlens)
+
+    @property
+    def n_real_rows(self) -> int:
+        return int(self.cu_seqlens_comp[-1])
+
+    @property
+    def width(self) -> int:
+        return self.coff * self.head_dim
+
+
+def offsets(seqlens, ratio: int, leading: int = 0):
+    """cu_seqlens (cumulative lengths, starting at ``leading``) and cu_seqlens_comp
+    (cumulative floor(len/ratio): each segment's tail tokens form no row)."""
+    cu = np.zeros(len(seqlens) + 1, dtype=np.int64)
+    cu[0] = leading
+    cu[1:] = leading + np.cumsum(np.asarray(seqlens, dtype=np.int64))
+    cc = np.zeros(len(seqlens) + 1, dtype=np.int64)
+    cc[1:] = np.cumsum(np.asarray(seqlens, dtype=np.int64) // ratio)
+    return cu.astype(np.int32), cc.astype(np.int32)
+
+
+def make_case(name, ratio, coff, head_dim, seqlens, capacity=None, extra_rows=0,
+              n_tokens=None, leading=0, seed=0, kv_scale=1.0, grad_scale=1.0,
+              score_sigma=1.5, ape_sigma=0.25) -> Case:
+    """Draw one case.  ``capacity`` defaults to the real row count + ``extra_rows``;
+    ``n_tokens`` defaults to cu_seqlens[-1] (no token padding)."""
+    cu, cc = offsets(seqlens, ratio, leading)
+    rows = int(cc[-1])
+    cap = rows + extra_rows if capacity is None else int(capacity)
+    T = int(cu[-1]) if n_tokens is None else int(n_tokens)
+    C = coff * head_dim
+    kv = to_bf16_bits(normal(seed, STREAM_KV, T * C) * kv_scale).reshape(T, C)
+    score = to_bf16_bits(normal(seed, STREAM_SCORE, T * C, score_sigma)).reshape(T, C)
+    ape = normal(seed, STREAM_APE, ratio * C, ape_sigma).astype(np.float32).reshape(ratio, C)
+    grad = to_bf16_bits(normal(seed, STREAM_GRAD, cap * head_dim) * grad_scale).reshape(cap, head_dim)
+    return Case(name, ratio, coff, head_dim, list(seqlens), cap, T, cu, cc, kv, score, ape, grad)
+
+
+# --- the workloads ---------------------------------------------------------
+
+def ragged_lengths(seed: int, n_seg: int = 64, max_len: int = 8192, ratio: int = 4,
+                   n_short: int = 4) -> list:
+    """Lengths uniform in [1, max_len]; then ``n_short`` distinct segments (chosen from
+    the same stream) are redrawn uniform in [1, ratio-1], so that some segments are
+    shorter than ratio (uniform draws alone almost never give one)."""
+    u = iter(uniform01(seed, STREAM_LENGTHS, n_seg + 64 * n_short + 64))
+    lens = [1 + int(next(u) * max_len) for _ in range(n_seg)]
+    picked = []
+    while len(picked) < min(n_short, n_seg):
+        idx = int(next(u) * n_seg)
+        if idx not in picked:
+            picked.append(idx)
+    for p in picked:
+        lens[p] = 1 + int(next(u) * (ratio - 1))
+    return lens
+
+
+def tiny(seed=0) -> Case:
+    """ratio 4, coff 2, head_dim 64, segments [37, 64], 3 padding rows."""
+    return make_case("tiny", 4, 2, 64, [37, 64], extra_rows=3, seed=seed)
+
+
+def uniform8x4096(seed=0) -> Case:
+    """ratio 4, coff 2, head_dim 512, 8 segments of 4096 tokens, capacity 8256."""
+    return make_case("r4c2d512_8x4096", 4, 2, 512, [4096] * 8, capacity=8256, seed=seed)
+
+
+def ragged64(seed=0) -> Case:
+    """ratio 4, coff 2, head_dim 512, 64 ragged segments, capacity = rows + 128."""
+    return make_case("r4c2d512_ragged64", 4, 2, 512, ragged_lengths(seed), extra_rows=128, seed=seed)
+
+
+def r128_4x32768(seed=0) -> Case:
+    """ratio 128, coff 1, head_dim 512, 4 segments of 32768 tokens (1024 rows)."""
+    return make_case("r128c1d512_4x32768", 128, 1, 512, [32768] * 4, seed=seed)
+
+
+def stress131072(seed=0, variant="unit") -> Case:
+    """ratio 4, coff 2, head_dim 512, one 131072-token segment.
+
+    variant "unit": the standard distributions; "x64": kv and grad_out scaled by 64;
+    "overflow": score = bf16 max and ape = fp32 max in columns {0, 1, D, D+1}."""
+    if variant == "x64":
+        return make_case("stress_x64", 4, 2, 512, [131072], seed=seed, kv_scale=64.0, grad_scale=64.0)
+    c = make_case("stress_" + variant, 4, 2, 512, [131072], seed=seed)
+    if variant == "overflow":
+        poison_columns(c, [0, 1, c.head_dim, c.head_dim + 1])
+    elif variant != "unit":
+        raise ValueError(variant)
+    return c
+
+
+def poison_columns(c: Case, cols) -> None:
+    """Overflow inputs: score = largest finite bf16 (0x7F7F) and ape = FLT_MAX in the
+    given packed columns, so that fp32 score + ape is +inf there."""
+    for col in cols:
+        c.score[:, col] = 0x7F7F
+        c.ape[:, col] = np.finfo(np.float32).max
+    c.name += "_cols" + "-".join(str(x) for x in cols)
+
+
+WORKLOADS = {
+    "tiny": tiny,
+    "r4c2d512_8x4096": uniform8x4096,
+    "r4c2d512_ragged64": ragged64,
+    "r128c1d512_4x32768": r128_4x32768,
+    "stress_unit": lambda seed=0: stress131072(seed, "unit"),
+    "stress_x64": lambda seed=0: stress131072(seed, "x64"),
+    "stress_overflow": lambda seed=0: stress131072(seed, "overflow"),
+}
