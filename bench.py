@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the CSA fused Compressor: one step = forward + backward over a
+THD pack (default: ratio 4, coff 2, head_dim 512, 8 segments of 4096 tokens,
+capacity 8256; seeded synthetic inputs from csa_workloads).
+
+Prints one JSON line.  `value` is input tokens per second of the whole step
+(forward + backward), summed over ranks, with inputs resident in HBM; the L2 is
+flushed (a 320 MB buffer write, outside the timed events) before every timed
+kernel call so that every call streams from HBM.  `e2e` is the same metric
+through the C ABI with pinned host buffers: host-to-device copies of the
+inputs, forward, backward and device-to-host copies of all outputs inside the
+timed region.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
+
+`--impl reference` times the CPU oracle (test infrastructure, unoptimised,
+single-threaded) on a bounded sample of the same workload; it is the baseline
+arm, not a target.  Under torchrun every rank runs an independent replica of
+the workload (weak scaling; the operator needs no data exchange: a data-
+parallel trainer all-reduces grad_ape with its other parameter gradients).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import csa_workloads as w  # noqa: E402
+
+METRIC = "CSA compressor fwd/bwd tokens/s and achieved HBM GB/s (% of GB300 peak)"
+L2_FLUSH_BYTES = 320 << 20
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="r4c2d512_8x4096", choices=sorted(w.WORKLOADS))
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--min-warmup-seconds", type=float, default=1.0,
+                   help="keep warming up at least this long (clock samples under load); 0 for profiling")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ bytes
+
+def algorithmic_bytes(c):
+    """Bytes each pass must move (each consumed kv/score slot read once; the
+    eager window materialisation is not counted).
+    forward:  kv + score of every consumed slot, ape, out (all capacity rows)
+    backward: kv + score of every consumed slot, grad_out of real rows, ape,
+              dkv + dscore written in full (n_tokens rows), dape written."""
+    nb = [L // c.ratio for L in c.seqlens]
+    consumed_rows = sum(b + (max(b - 1, 0) if c.coff == 2 else 0) for b in nb)  # half-rows of D
+    win = 4 * c.head_dim * c.ratio * consumed_rows
+    C = c.coff * c.head_dim
+    ape = 4 * c.ratio * C
+    fwd = win + ape + 2 * c.capacity * c.head_dim
+    bwd = win + 2 * c.n_real_rows * c.head_dim + ape + 4 * c.n_tokens * C + ape
+    return fwd, bwd
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        busy = [x for x in sm if x > 0.5 * max(sm)]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu capture, only if the kernel
+    sources are unchanged since (same hash); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for rel in rec["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return rec["bytes_per_launch"] if h.hexdigest() == rec["sha256"] else None
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import sparse_attention_kv_csa_gb300 as csa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    c = w.WORKLOADS[args.workload](seed=rank)
+    C = c.coff * c.head_dim
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    kv, sc, ape = up(c.kv), up(c.score), up(c.ape)
+    cu, cc, g = up(c.cu_seqlens), up(c.cu_seqlens_comp), up(c.grad_out)
+    out = torch.empty((c.capacity, c.head_dim), dtype=torch.int16, device=dev)
+    dkv = torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev)
+    dsc = torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev)
+    dape = torch.empty((c.ratio, C), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def fwd():
+        csa.csa_compress_fwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity, out, stream)
+
+    def bwd():
+        csa.csa_compress_bwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity,
+                             c.n_tokens, g, dkv, dsc, dape, stream)
+
+    def timed(fn, ev0, ev1):
+        flush.zero_()
+        ev0.record(stream)
+        fn()
+        ev1.record(stream)
+
+    sampler = ClockSampler(local_rank) if rank == 0 and not args.no_clocks else None
+    if sampler:
+        sampler.start()
+    # warm-up: at least W steps and about a second, so that the clock samples
+    # below are taken under this workload
+    t_end = time.time() + args.min_warmup_seconds
+    n = 0
+    while n < args.warmup or time.time() < t_end:
+        flush.zero_()
+        fwd()
+        flush.zero_()
+        bwd()
+        n += 1
+        if n % 10 == 0:
+            torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    for e in evs:
+        timed(fwd, e[0], e[1])
+        timed(bwd, e[2], e[3])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    t_fwd = [e[0].elapsed_time(e[1]) for e in evs]
+    t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
+    ms_fwd, ms_bwd = sum(t_fwd) / len(t_fwd), sum(t_bwd) / len(t_bwd)
+    ms_step = ms_fwd + ms_bwd
+    if world > 1:
+        t = torch.tensor([ms_step, ms_fwd, ms_bwd], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_fwd, ms_bwd = [float(x) for x in t.cpu()]
+
+    e2e = None if args.no_e2e else run_e2e(args, c, csa, dev, stream, world)
+    return c, ms_step, ms_fwd, ms_bwd, clocks, e2e
+
+
+def run_e2e(args, c, csa, dev, stream, world):
+    """Same step through the C ABI from pinned host buffers: H2D inputs, forward,
+    backward, D2H outputs, all inside the timed region."""
+    import torch
+    C = c.coff * c.head_dim
+
+    def pin(a):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.pin_memory()
+
+    h_in = [pin(c.kv), pin(c.score), pin(c.ape), pin(c.cu_seqlens), pin(c.cu_seqlens_comp), pin(c.grad_out)]
+    d_in = [torch.empty_like(t, device=dev) for t in h_in]
+    d_out = [torch.empty((c.capacity, c.head_dim), dtype=torch.int16, device=dev),
+             torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev),
+             torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev),
+             torch.empty((c.ratio, C), dtype=torch.float32, device=dev)]
+    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in d_out]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def step():
+        for d, h in zip(d_in, h_in):
+            d.copy_(h, non_blocking=True)
+        kv, sc, ape, cu, cc, g = d_in
+        out, dkv, dsc, dape = d_out
+        csa.csa_compress_fwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity, out, stream)
+        csa.csa_compress_bwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity,
+                             c.n_tokens, g, dkv, dsc, dape, stream)
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k = max(3, min(args.steps, 20))
+    e0.record(stream)
+    for _ in range(k):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / k
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": world * c.n_tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(c, target_s):
+    """Times the oracle's fp32 forward + backward on the first segments of the
+    workload, adding segments until about target_s seconds of CPU work."""
+    import oracle
+    oracle.build()
+    done_tokens, spent, nseg = 0, 0.0, 0
+    while spent < target_s and nseg < len(c.seqlens):
+        nseg += 1
+        lens = c.seqlens[:nseg]
+        s = w.make_case("sample", c.ratio, c.coff, c.head_dim, lens, seed=0)
+        t0 = time.perf_counter()
+        oracle.case_fwd_f32(s)
+        oracle.case_bwd_f32(s)
+        spent += time.perf_counter() - t0
+        done_tokens += s.n_tokens
+    return done_tokens, spent, nseg
+
+
+def cpu_baseline(c, target_s):
+    tokens, spent, nseg = oracle_sample(c, target_s)
+    return {"value": tokens / spent, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": "fp32 oracle fwd+bwd on growing prefixes of the pack (1..%d of %d segments, "
+                      "%d tokens, %.1f s)" % (nseg, len(c.seqlens), tokens, spent)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    spec = w.SPECS[args.workload](0)
+    # one step = fp32 oracle forward + backward on one segment of the pack
+    s = w.make_case("sample", spec["ratio"], spec["coff"], spec["head_dim"], spec["seqlens"][:1], seed=0)
+    for _ in range(args.warmup):
+        oracle.case_fwd_f32(s)
+        oracle.case_bwd_f32(s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.case_fwd_f32(s)
+        oracle.case_bwd_f32(s)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = s.n_tokens / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": spec["name"], "sample": "one %d-token segment of the pack per step" % s.n_tokens},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": "fp32 oracle fwd+bwd, one %d-token segment per step" % s.n_tokens},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    c, ms_step, ms_fwd, ms_bwd, clocks, e2e = run_ours(args, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+    fwd_b, bwd_b = algorithmic_bytes(c)
+    peak, peak_kind = measured_peak()
+    tokens = c.n_tokens
+    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * tokens / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": c.name, "ratio": c.ratio, "coff": c.coff, "head_dim": c.head_dim,
+                   "segments": len(c.seqlens), "tokens": tokens, "rows": c.n_real_rows,
+                   "capacity": c.capacity, "l2": "flushed (320 MB write) before every timed call",
+                   "inputs": "bf16 kv/score/grad_out, fp32 ape; fp32 arithmetic"},
+        "fwd": {"ms": ms_fwd, "tokens_per_s": world * tokens / (ms_fwd * 1e-3), "bytes": fwd_b,
+                "gbs": gbs(fwd_b, ms_fwd), "frac_of_peak": gbs(fwd_b, ms_fwd) / peak},
+        "bwd": {"ms": ms_bwd, "tokens_per_s": world * tokens / (ms_bwd * 1e-3), "bytes": bwd_b,
+                "gbs": gbs(bwd_b, ms_bwd), "frac_of_peak": gbs(bwd_b, ms_bwd) / peak},
+        "roofline": {"bound": "hbm", "kernel": "csa_compress_bwd (bwd_small_kernel + dape_finalize_kernel)",
+                     "achieved": gbs(bwd_b, ms_bwd), "peak": peak, "peak_source": peak_kind + " hbm_gbs",
+                     "unit": "GB/s", "frac": gbs(bwd_b, ms_bwd) / peak,
+                     "traffic": recorded_traffic("bwd_small_kernel:" + c.name)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(c, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -9,8 +9,10 @@ Random numbers come from SplitMix64 (Steele, Lea and Flood, "Fast splittable
 pseudorandom number generators", OOPSLA 2014) run as a counter-based generator
 (value i of stream ``seed`` is the SplitMix64 finaliser of ``seed*GOLDEN +
 (i+1)*GOLDEN``), turned into normals with the Box-Muller transform and rounded
-to bf16 with round-to-nearest-even.  Everything is numpy, so the same seed
-gives the same bits on x86_64 and aarch64.
+to bf16 with round-to-nearest-even.  The uniform draws are bit-identical on
+every platform; the normals go through the platform's log/sqrt/cos/sin, which
+may differ in a last fp64 ulp between machines (rarely moving a bf16 rounding).
+Tests always draw oracle and GPU inputs in the same process.
 
 Distributions follow the Numerics section of the "CSA Fused Compressor" page
 (cuDNN frontend docs): kv, grad_out ~ N(0, 1) bf16, score ~ N(0, 1.5^2) bf16,
@@ -52,25 +54,35 @@ def uniform01(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
     return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
 
 
-def normal(seed: int, stream: int, n: int, sigma: float = 1.0) -> np.ndarray:
-    """n N(0, sigma^2) doubles by Box-Muller (two uniforms per pair)."""
+def normal(seed: int, stream: int, n: int, sigma: float = 1.0, chunk: int = 1 << 20) -> np.ndarray:
+    """n N(0, sigma^2) doubles by Box-Muller: draws 2i and 2i+1 of the stream give
+    normals 2i (cosine) and 2i+1 (sine).  Computed in chunks to stay cache-sized."""
     m = (n + 1) // 2
-    u = uniform01(seed, stream, 2 * m)
-    u1, u2 = u[0::2], u[1::2]
-    rad = np.sqrt(-2.0 * np.log(u1))
-    ang = 2.0 * np.pi * u2
     z = np.empty(2 * m, dtype=np.float64)
-    z[0::2] = rad * np.cos(ang)
-    z[1::2] = rad * np.sin(ang)
-    return z[:n] * sigma
+    for s0 in range(0, m, chunk):
+        s1 = min(m, s0 + chunk)
+        u = uniform01(seed, stream, 2 * (s1 - s0), offset=2 * s0)
+        rad = np.sqrt(-2.0 * np.log(u[0::2]))
+        ang = 2.0 * np.pi * u[1::2]
+        z[2 * s0:2 * s1:2] = rad * np.cos(ang)
+        z[2 * s0 + 1:2 * s1:2] = rad * np.sin(ang)
+    z = z[:n]
+    if sigma != 1.0:
+        z *= sigma
+    return z
 
 
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
-    f = np.ascontiguousarray(x, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    nan = (u & 0x7FFFFFFF) > 0x7F800000
-    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    f = np.array(x, dtype=np.float32, copy=True, order="C")
+    u = f.view(np.uint32)
+    nan = np.isnan(f)
+    lsb = u >> np.uint32(16)
+    lsb &= np.uint32(1)
+    lsb += np.uint32(0x7FFF)
+    u += lsb  # no wrap: the largest non-NaN pattern is 0xFF800000 (-inf)
+    u >>= np.uint32(16)
+    r = u.astype(np.uint16)
     r[nan] = 0x7FC0
     return r
 
@@ -157,39 +169,52 @@ def ragged_lengths(seed: int, n_seg: int = 64, max_len: int = 8192, ratio: int =
     return lens
 
 
+# Each workload as make_case keyword arguments (shapes only, no data drawn).
+SPECS = {
+    # ratio 4, coff 2, head_dim 64, segments [37, 64], 3 padding rows
+    "tiny": lambda seed=0: dict(name="tiny", ratio=4, coff=2, head_dim=64, seqlens=[37, 64], extra_rows=3),
+    # ratio 4, coff 2, head_dim 512, 8 segments of 4096 tokens, capacity 8256
+    "r4c2d512_8x4096": lambda seed=0: dict(name="r4c2d512_8x4096", ratio=4, coff=2, head_dim=512,
+                                           seqlens=[4096] * 8, capacity=8256),
+    # ratio 4, coff 2, head_dim 512, 64 ragged segments, capacity = rows + 128
+    "r4c2d512_ragged64": lambda seed=0: dict(name="r4c2d512_ragged64", ratio=4, coff=2, head_dim=512,
+                                             seqlens=ragged_lengths(seed), extra_rows=128),
+    # ratio 128, coff 1, head_dim 512, 4 segments of 32768 tokens (1024 rows)
+    "r128c1d512_4x32768": lambda seed=0: dict(name="r128c1d512_4x32768", ratio=128, coff=1, head_dim=512,
+                                              seqlens=[32768] * 4),
+    # ratio 4, coff 2, head_dim 512, one 131072-token segment: unit scale, kv and
+    # grad_out x64, and fp32 overflow (see poison_columns)
+    "stress_unit": lambda seed=0: dict(name="stress_unit", ratio=4, coff=2, head_dim=512, seqlens=[131072]),
+    "stress_x64": lambda seed=0: dict(name="stress_x64", ratio=4, coff=2, head_dim=512, seqlens=[131072],
+                                      kv_scale=64.0, grad_scale=64.0),
+    "stress_overflow": lambda seed=0: dict(name="stress_overflow", ratio=4, coff=2, head_dim=512,
+                                           seqlens=[131072]),
+}
+
+
+def build(name: str, seed: int = 0) -> Case:
+    kw = SPECS[name](seed)
+    nm = kw.pop("name")
+    c = make_case(nm, seed=seed, **kw)
+    if name == "stress_overflow":
+        poison_columns(c, [0, 1, c.head_dim, c.head_dim + 1])
+    return c
+
+
 def tiny(seed=0) -> Case:
-    """ratio 4, coff 2, head_dim 64, segments [37, 64], 3 padding rows."""
-    return make_case("tiny", 4, 2, 64, [37, 64], extra_rows=3, seed=seed)
+    return build("tiny", seed)
 
 
 def uniform8x4096(seed=0) -> Case:
-    """ratio 4, coff 2, head_dim 512, 8 segments of 4096 tokens, capacity 8256."""
-    return make_case("r4c2d512_8x4096", 4, 2, 512, [4096] * 8, capacity=8256, seed=seed)
+    return build("r4c2d512_8x4096", seed)
 
 
 def ragged64(seed=0) -> Case:
-    """ratio 4, coff 2, head_dim 512, 64 ragged segments, capacity = rows + 128."""
-    return make_case("r4c2d512_ragged64", 4, 2, 512, ragged_lengths(seed), extra_rows=128, seed=seed)
+    return build("r4c2d512_ragged64", seed)
 
 
 def r128_4x32768(seed=0) -> Case:
-    """ratio 128, coff 1, head_dim 512, 4 segments of 32768 tokens (1024 rows)."""
-    return make_case("r128c1d512_4x32768", 128, 1, 512, [32768] * 4, seed=seed)
-
-
-def stress131072(seed=0, variant="unit") -> Case:
-    """ratio 4, coff 2, head_dim 512, one 131072-token segment.
-
-    variant "unit": the standard distributions; "x64": kv and grad_out scaled by 64;
-    "overflow": score = bf16 max and ape = fp32 max in columns {0, 1, D, D+1}."""
-    if variant == "x64":
-        return make_case("stress_x64", 4, 2, 512, [131072], seed=seed, kv_scale=64.0, grad_scale=64.0)
-    c = make_case("stress_" + variant, 4, 2, 512, [131072], seed=seed)
-    if variant == "overflow":
-        poison_columns(c, [0, 1, c.head_dim, c.head_dim + 1])
-    elif variant != "unit":
-        raise ValueError(variant)
-    return c
+    return build("r128c1d512_4x32768", seed)
 
 
 def poison_columns(c: Case, cols) -> None:
@@ -201,12 +226,8 @@ def poison_columns(c: Case, cols) -> None:
     c.name += "_cols" + "-".join(str(x) for x in cols)
 
 
-WORKLOADS = {
-    "tiny": tiny,
-    "r4c2d512_8x4096": uniform8x4096,
-    "r4c2d512_ragged64": ragged64,
-    "r128c1d512_4x32768": r128_4x32768,
-    "stress_unit": lambda seed=0: stress131072(seed, "unit"),
-    "stress_x64": lambda seed=0: stress131072(seed, "x64"),
-    "stress_overflow": lambda seed=0: stress131072(seed, "overflow"),
-}
+class _Workloads(dict):
+    """name -> callable(seed=0) drawing that workload."""
+
+
+WORKLOADS = _Workloads({name: (lambda name: (lambda seed=0: build(name, seed)))(name) for name in SPECS})

@@ -1,0 +1,143 @@
+/*
+ * csa.h -- C ABI of libcsa, the GB300 (sm_103a) CSA/HCA fused Compressor.
+ *
+ * The operation ("CSA Fused Compressor", cuDNN frontend docs, section Semantics):
+ * for each THD segment s = [cu_seqlens[s], cu_seqlens[s+1]) and each of its
+ * floor(len/ratio) blocks b of ratio tokens (the segment's tail tokens are
+ * dropped), output row r = cu_seqlens_comp[s] + b is
+ *
+ *     out[r, j] = sum_k kv[w(b,k), c(k,j)] * softmax_k(score[w(b,k), c(k,j)]
+ *                                                      + ape[k % ratio, c(k,j)])
+ *
+ * with, for coff == 2 (overlapping form, window 2*ratio): k < ratio -> the previous
+ * block's token, column c = j (first half), invalid for a segment's first block;
+ * k >= ratio -> the own block's token, column c = head_dim + j (second half).
+ * For coff == 1 (own-block form, window ratio): the own block's token, column j.
+ * Rows r in [cu_seqlens_comp[n_seg], capacity) are padding rows computed as a
+ * first block starting at token 0; the backward ignores grad_out on them.
+ * Arithmetic is fp32 with a single final bf16 rounding (section Numerics).
+ *
+ * Layouts (THD packed, row-major, contiguous; section API Usage):
+ *   kv, score      bf16  [n_tokens, coff*head_dim]
+ *   ape            fp32  [ratio, coff*head_dim]
+ *   cu_seqlens     int32 [n_seg + 1]  token offsets, nondecreasing
+ *   cu_seqlens_comp int32 [n_seg + 1] row offsets: cu_seqlens_comp[0] == 0 and
+ *                  cu_seqlens_comp[s+1] - cu_seqlens_comp[s] == floor(len_s / ratio)
+ *   out, grad_out  bf16  [capacity, head_dim]
+ *   dkv, dscore    bf16  [n_tokens, coff*head_dim]
+ *   dape           fp32  [ratio, coff*head_dim]
+ * bf16 tensors are passed as raw 16-bit patterns (void*).
+ *
+ * Ownership and memory: every pointer is a device pointer on the current CUDA
+ * device, owned by the caller, valid until the stream has finished the call's
+ * work.  Tensor bases must be 16-byte aligned (the int32 offsets 4-byte aligned);
+ * this is checked on every call.  The library keeps no per-call state.  `stream`
+ * is a cudaStream_t (NULL = the legacy default stream).  Calls are asynchronous:
+ * no call synchronises the device or reads device memory on the host.
+ *
+ * Trusted device contents: the offsets in cu_seqlens / cu_seqlens_comp are not
+ * validated (that would need a device-to-host read).  The caller guarantees the
+ * relations above, capacity >= cu_seqlens_comp[n_seg], and that kv / score hold at
+ * least cu_seqlens[n_seg] rows (and at least ratio rows when capacity > 0).
+ *
+ * Errors: every entry point returns CSA_OK (0) or a csa_status below.  A failed
+ * validation launches nothing and touches no output.  No C++ exception crosses
+ * the ABI.  csa_last_error_message() gives a thread-local description of the
+ * calling thread's last non-OK return.
+ *
+ * Supported set (csa_check_support): coff in {1, 2}; ratio == 4 with head_dim a
+ * multiple of 8 in [8, 8192].
+ */
+#ifndef CSA_H_
+#define CSA_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSA_API __attribute__((visibility("default")))
+#else
+#define CSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum csa_status {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_VALUE = 1,   /* null pointer, negative size, coff not in {1,2}, ...   */
+    CSA_ERR_UNSUPPORTED = 2,     /* (ratio, coff, head_dim) outside the kernel set        */
+    CSA_ERR_MISALIGNED = 3,      /* a tensor base not 16-byte (offsets: 4-byte) aligned   */
+    CSA_ERR_TOO_LARGE = 4,       /* a flat element offset would not fit in int32          */
+    CSA_ERR_CUDA = 5,            /* a CUDA runtime call or kernel launch failed           */
+    CSA_ERR_OUT_OF_MEMORY = 6,   /* the backward's stream-ordered workspace allocation    */
+    CSA_ERR_DEVICE_TIMEOUT = 7   /* a bounded device-side wait expired (see below)        */
+} csa_status;
+
+/*
+ * Forward pass ("CSA Fused Compressor", sections Semantics and API Usage: the
+ * forward wrapper with an explicit static total_comp = capacity).
+ *
+ * Writes out[0, capacity) x [0, head_dim) in full, padding rows included.
+ * Reads kv / score rows of real blocks (and their previous blocks for coff == 2)
+ * and rows [0, ratio) when capacity exceeds the real row count.
+ * capacity == 0: nothing is launched and CSA_OK is returned; the tensor pointers
+ * may then be NULL.  Bitwise deterministic.
+ */
+CSA_API int csa_compress_fwd(const void *kv, const void *score, const float *ape,
+                     const int32_t *cu_seqlens, const int32_t *cu_seqlens_comp, int32_t n_seg,
+                     int32_t ratio, int32_t coff, int32_t head_dim, int32_t capacity,
+                     void *out, void *stream);
+
+/*
+ * Backward pass ("CSA Fused Compressor", Semantics: the chain rule through the
+ * pooling; Class API: gradient buffers may be uninitialised because every slot
+ * is written, never-consumed slots with exact zeros).
+ *
+ * n_tokens: rows of kv / score / dkv / dscore.  If n_tokens < 0 the library uses
+ * cu_seqlens[n_seg], read on the device (token padding rows past it are then left
+ * untouched).  Writes:
+ *   dkv, dscore  all of [0, n_tokens) x [0, coff*head_dim): the gradient at every
+ *                slot a real row reads, +0 at every other slot (segment tails,
+ *                the last block's first-half columns when coff == 2, segments
+ *                shorter than ratio, tokens outside the segments);
+ *   dape         overwritten (not accumulated) with the sum over real rows, formed
+ *                as fixed-order partial sums: no atomics, bitwise reproducible
+ *                run to run.
+ * grad_out rows at or past cu_seqlens_comp[n_seg] are ignored.
+ * Scratch: grad_ape partials (a few MB at most) come from a library-owned,
+ * stream-ordered memory pool on the current device, allocated and released in
+ * stream order inside the call.  capacity == 0 still writes dkv / dscore zeros
+ * and dape = 0.  Errors as above; CSA_ERR_OUT_OF_MEMORY if the workspace cannot
+ * be allocated.
+ */
+CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape,
+                     const int32_t *cu_seqlens, const int32_t *cu_seqlens_comp, int32_t n_seg,
+                     int32_t ratio, int32_t coff, int32_t head_dim, int32_t capacity,
+                     int64_t n_tokens, const void *grad_out, void *dkv, void *dscore,
+                     float *dape, void *stream);
+
+/*
+ * Host-only support check ("CSA Fused Compressor", section Support surface):
+ * CSA_OK if (ratio, coff, head_dim) has a kernel and the sizes fit the int32
+ * flat-offset bounds (n_tokens * coff * head_dim < 2^31, capacity * head_dim <
+ * 2^31); capacity > 0 requires n_tokens >= ratio.  n_tokens < 0 skips the
+ * checks that need it.  Makes no CUDA call.
+ */
+CSA_API int csa_check_support(int32_t ratio, int32_t coff, int32_t head_dim, int64_t n_tokens,
+                      int32_t capacity);
+
+/* Static string naming a status code.  Never NULL. */
+CSA_API const char *csa_status_string(int status);
+
+/* Thread-local text of the calling thread's last non-OK return ("" if none). */
+CSA_API const char *csa_last_error_message(void);
+
+/* Library version as an integer: major * 10000 + minor * 100 + patch. */
+CSA_API int csa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H_ */

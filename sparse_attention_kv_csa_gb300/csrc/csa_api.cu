@@ -1,0 +1,230 @@
+// C-ABI entry points of libcsa (declared in include/csa.h): argument validation,
+// kernel-family dispatch and the backward's stream-ordered workspace.
+//
+// Validation follows the support surface of the "CSA Fused Compressor" page
+// (cuDNN frontend docs, section Support surface): coff in {1, 2}, supported
+// (ratio, head_dim), int32 flat offsets, total_comp > 0 requiring at least ratio
+// tokens, 16-byte aligned tensor bases (4-byte for the int32 offsets) checked per
+// call.  Nothing is launched and no output is touched when validation fails.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "csa.h"
+#include "csa_launch.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(e == cudaErrorMemoryAllocation ? CSA_ERR_OUT_OF_MEMORY : CSA_ERR_CUDA, "%s: %s (%s)",
+                what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int64_t kInt32Limit = int64_t(1) << 31;
+constexpr int kMaxDevices = 64;
+
+// Per-device facts and the workspace pool, created on first use on that device.
+struct DeviceState {
+    std::once_flag once;
+    cudaError_t init_err = cudaSuccess;
+    int num_sms = 0;
+    cudaMemPool_t pool = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+cudaError_t device_state(DeviceState **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    DeviceState &d = g_dev[dev];
+    std::call_once(d.once, [&d, dev]() {
+        cudaError_t err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (err == cudaSuccess) {
+            // A pool of its own, so that the workspace stays cached between calls
+            // without changing the device's default pool.
+            cudaMemPoolProps props;
+            memset(&props, 0, sizeof(props));
+            props.allocType = cudaMemAllocationTypePinned;
+            props.handleTypes = cudaMemHandleTypeNone;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            err = cudaMemPoolCreate(&d.pool, &props);
+            if (err == cudaSuccess) {
+                uint64_t keep = 256ull << 20;
+                err = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            }
+        }
+        d.init_err = err;
+    });
+    *out = &d;
+    return d.init_err;
+}
+
+int check_common(int32_t n_seg, int32_t ratio, int32_t coff, int32_t head_dim, int32_t capacity)
+{
+    if (n_seg < 0)
+        return fail(CSA_ERR_INVALID_VALUE, "n_seg must be >= 0 (got %d)", n_seg);
+    if (capacity < 0)
+        return fail(CSA_ERR_INVALID_VALUE, "capacity must be >= 0 (got %d)", capacity);
+    if (coff != 1 && coff != 2)
+        return fail(CSA_ERR_INVALID_VALUE, "coff must be 1 or 2 (got %d)", coff);
+    if (ratio < 1)
+        return fail(CSA_ERR_INVALID_VALUE, "ratio must be >= 1 (got %d)", ratio);
+    if (head_dim < 1)
+        return fail(CSA_ERR_INVALID_VALUE, "head_dim must be >= 1 (got %d)", head_dim);
+    if (ratio == 4) {
+        if (head_dim % 8 != 0 || head_dim > 8192)
+            return fail(CSA_ERR_UNSUPPORTED,
+                        "ratio 4 needs head_dim a multiple of 8 in [8, 8192] (got %d)", head_dim);
+    } else {
+        return fail(CSA_ERR_UNSUPPORTED, "ratio %d has no kernel (supported: 4)", ratio);
+    }
+    if ((int64_t)capacity * head_dim >= kInt32Limit)
+        return fail(CSA_ERR_TOO_LARGE, "capacity * head_dim = %lld does not fit int32 offsets",
+                    (long long)capacity * head_dim);
+    return CSA_OK;
+}
+
+int check_tokens(int32_t ratio, int32_t coff, int32_t head_dim, int64_t n_tokens, int32_t capacity)
+{
+    if (n_tokens < 0)
+        return CSA_OK;
+    if (n_tokens * coff * (int64_t)head_dim >= kInt32Limit)
+        return fail(CSA_ERR_TOO_LARGE, "n_tokens * coff * head_dim = %lld does not fit int32 offsets",
+                    (long long)(n_tokens * coff * (int64_t)head_dim));
+    if (capacity > 0 && n_tokens < ratio)
+        return fail(CSA_ERR_INVALID_VALUE,
+                    "capacity > 0 needs n_tokens >= ratio (each row reads ratio tokens); got %lld < %d",
+                    (long long)n_tokens, ratio);
+    return CSA_OK;
+}
+
+int check_ptr(const void *p, const char *name, uintptr_t align)
+{
+    if (!p)
+        return fail(CSA_ERR_INVALID_VALUE, "%s is NULL", name);
+    if (!aligned(p, align))
+        return fail(CSA_ERR_MISALIGNED, "%s = %p is not %d-byte aligned", name, p, (int)align);
+    return CSA_OK;
+}
+
+#define CSA_TRY(expr)               \
+    do {                            \
+        int rc_ = (expr);           \
+        if (rc_ != CSA_OK)          \
+            return rc_;             \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int csa_version(void) { return 100; }
+
+const char *csa_status_string(int status)
+{
+    switch (status) {
+    case CSA_OK: return "CSA_OK";
+    case CSA_ERR_INVALID_VALUE: return "CSA_ERR_INVALID_VALUE";
+    case CSA_ERR_UNSUPPORTED: return "CSA_ERR_UNSUPPORTED";
+    case CSA_ERR_MISALIGNED: return "CSA_ERR_MISALIGNED";
+    case CSA_ERR_TOO_LARGE: return "CSA_ERR_TOO_LARGE";
+    case CSA_ERR_CUDA: return "CSA_ERR_CUDA";
+    case CSA_ERR_OUT_OF_MEMORY: return "CSA_ERR_OUT_OF_MEMORY";
+    case CSA_ERR_DEVICE_TIMEOUT: return "CSA_ERR_DEVICE_TIMEOUT";
+    default: return "CSA_ERR_UNKNOWN";
+    }
+}
+
+const char *csa_last_error_message(void) { return g_msg; }
+
+int csa_check_support(int32_t ratio, int32_t coff, int32_t head_dim, int64_t n_tokens, int32_t capacity)
+{
+    CSA_TRY(check_common(0, ratio, coff, head_dim, capacity));
+    CSA_TRY(check_tokens(ratio, coff, head_dim, n_tokens, capacity));
+    return CSA_OK;
+}
+
+int csa_compress_fwd(const void *kv, const void *score, const float *ape, const int32_t *cu_seqlens,
+                     const int32_t *cu_seqlens_comp, int32_t n_seg, int32_t ratio, int32_t coff,
+                     int32_t head_dim, int32_t capacity, void *out, void *stream)
+{
+    CSA_TRY(check_common(n_seg, ratio, coff, head_dim, capacity));
+    CSA_TRY(check_ptr(cu_seqlens, "cu_seqlens", 4));
+    CSA_TRY(check_ptr(cu_seqlens_comp, "cu_seqlens_comp", 4));
+    if (capacity == 0)
+        return CSA_OK;
+    CSA_TRY(check_ptr(kv, "kv", 16));
+    CSA_TRY(check_ptr(score, "score", 16));
+    CSA_TRY(check_ptr(ape, "ape", 16));
+    CSA_TRY(check_ptr(out, "out", 16));
+    csa::FwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim, capacity, out};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = csa::launch_fwd_small(p, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "forward launch");
+    return CSA_OK;
+}
+
+int csa_compress_bwd(const void *kv, const void *score, const float *ape, const int32_t *cu_seqlens,
+                     const int32_t *cu_seqlens_comp, int32_t n_seg, int32_t ratio, int32_t coff,
+                     int32_t head_dim, int32_t capacity, int64_t n_tokens, const void *grad_out,
+                     void *dkv, void *dscore, float *dape, void *stream)
+{
+    CSA_TRY(check_common(n_seg, ratio, coff, head_dim, capacity));
+    CSA_TRY(check_tokens(ratio, coff, head_dim, n_tokens, capacity));
+    CSA_TRY(check_ptr(cu_seqlens, "cu_seqlens", 4));
+    CSA_TRY(check_ptr(cu_seqlens_comp, "cu_seqlens_comp", 4));
+    if (capacity > 0) {
+        CSA_TRY(check_ptr(kv, "kv", 16));
+        CSA_TRY(check_ptr(score, "score", 16));
+        CSA_TRY(check_ptr(ape, "ape", 16));
+        CSA_TRY(check_ptr(grad_out, "grad_out", 16));
+    }
+    if (n_tokens != 0) {
+        CSA_TRY(check_ptr(dkv, "dkv", 16));
+        CSA_TRY(check_ptr(dscore, "dscore", 16));
+    }
+    CSA_TRY(check_ptr(dape, "dape", 16));
+
+    DeviceState *ds = nullptr;
+    cudaError_t e = device_state(&ds);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device set-up");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
+                     capacity, n_tokens, grad_out, dkv, dscore, dape};
+    const csa::SmallBwdPlan pl = csa::plan_bwd_small(ratio, coff, head_dim, capacity, ds->num_sms);
+    void *partial = nullptr;
+    e = cudaMallocFromPoolAsync(&partial, (size_t)pl.partial_floats * sizeof(float), ds->pool, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "backward workspace");
+    e = csa::launch_bwd_small(p, pl, static_cast<float *>(partial), st);
+    cudaError_t e2 = cudaFreeAsync(partial, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "backward launch");
+    if (e2 != cudaSuccess)
+        return cuda_fail(e2, "backward workspace release");
+    return CSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,143 @@
+// Device helpers shared by the Compressor kernels: packed fp32 pair arithmetic,
+// the library's own exp, bf16 conversion and the row -> segment map.
+//
+// Numerics ("CSA Fused Compressor", cuDNN frontend docs, section Numerics): all
+// window arithmetic is fp32 with one final bf16 rounding, and every add, multiply
+// and fused multiply-add is an explicit round-to-nearest instruction, so nothing
+// depends on the compiler contracting a*b+c.  The library is built without
+// --use_fast_math: no flush-to-zero, IEEE division and reciprocal.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace csa {
+
+// ------------------------------------------------------------ fp32 pairs
+// Two fp32 lanes in one float2, computed with the sm_100+ packed instructions
+// (two results per issue slot).  Each lane rounds exactly like the scalar op.
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 splat(float v) { return make_float2(v, v); }
+
+// max that returns NaN when either input is NaN.
+__device__ __forceinline__ float max_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// ------------------------------------------------------------------ exp
+// e^x for x <= 0 (or NaN), the library's own: Cody-Waite reduction (Cody and
+// Waite, "Software Manual for the Elementary Functions", 1980) x = n ln2 + r with
+// ln2 split in two parts, |r| <= ln2/2; e^r by its degree-7 Taylor polynomial in
+// Horner form; 2^n put into the exponent field.  Results below 2^-126.5 are +0
+// (n = -127 gives a zero scale); NaN propagates.  Constants from their definitions:
+//   kLog2e = 1/ln2 to fp32; kLn2Hi = ln2 cut to a 16-bit significand (so n*kLn2Hi
+//   is exact); kLn2Lo = ln2 - kLn2Hi to fp32; kRound = 1.5*2^23 (adding it leaves
+//   nearest(y) in the low significand bits); kInvFact[k] = 1/k! to fp32.
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kLn2Hi = 0.693145751953125f;
+constexpr float kLn2Lo = 1.42860682030941723212e-6f;
+constexpr float kRound = 12582912.0f;
+constexpr float kExpFloor = -88.0f;
+constexpr float kInvFact2 = 1.0f / 2.0f;
+constexpr float kInvFact3 = 1.0f / 6.0f;
+constexpr float kInvFact4 = 1.0f / 24.0f;
+constexpr float kInvFact5 = 1.0f / 120.0f;
+constexpr float kInvFact6 = 1.0f / 720.0f;
+constexpr float kInvFact7 = 1.0f / 5040.0f;
+
+__device__ __forceinline__ float2 exp2lanes(float2 x)
+{
+    x.x = max_nan(x.x, kExpFloor);
+    x.y = max_nan(x.y, kExpFloor);
+    const float2 t = fma2(x, splat(kLog2e), splat(kRound));   // kRound + n
+    const float2 n = add2(t, splat(-kRound));                  // n, exact
+    float2 r = fma2(n, splat(-kLn2Hi), x);
+    r = fma2(n, splat(-kLn2Lo), r);
+    float2 p = fma2(splat(kInvFact7), r, splat(kInvFact6));
+    p = fma2(p, r, splat(kInvFact5));
+    p = fma2(p, r, splat(kInvFact4));
+    p = fma2(p, r, splat(kInvFact3));
+    p = fma2(p, r, splat(kInvFact2));
+    p = fma2(p, r, splat(1.0f));
+    p = fma2(p, r, splat(1.0f));
+    // bits(t) = bits(kRound) + n; bits(kRound) << 23 vanishes mod 2^32, so
+    // (bits(t) << 23) + bias is the bit pattern of 2^n (and +0 for n = -127).
+    const float2 scale = make_float2(__uint_as_float(__float_as_uint(t.x) * 8388608u + 0x3f800000u),
+                                     __uint_as_float(__float_as_uint(t.y) * 8388608u + 0x3f800000u));
+    return mul2(p, scale);
+}
+
+// ----------------------------------------------------------------- bf16
+// A 32-bit word holding two bf16 (low half = lower column) <-> an fp32 pair.
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Round an fp32 pair to bf16, nearest-even (cvt.rn), lower column in the low half.
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float2 v)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ------------------------------------------------------------- row map
+// Output row r is block b = r - cu_seqlens_comp[s] of the segment s with
+// cu_seqlens_comp[s] <= r < cu_seqlens_comp[s+1]; its own tokens start at
+// cu_seqlens[s] + b*ratio.  Rows outside [cu_seqlens_comp[0], cu_seqlens_comp[n_seg])
+// are padding rows: a first block starting at token 0 ("CSA Fused Compressor",
+// Semantics: rows beyond cu_seqlens_comp[-1] use first-in-segment semantics from
+// token 0).
+struct RowMap {
+    int64_t base;
+    int seg;
+    bool real;
+    bool first;
+};
+
+__device__ __forceinline__ int find_segment(const int32_t *__restrict__ cc, int n_seg, int r)
+{
+    int lo = 0, hi = n_seg;  // cc[lo] <= r < cc[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(cc + mid) <= r)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ RowMap map_row(int r, const int32_t *__restrict__ cu,
+                                          const int32_t *__restrict__ cc, int n_seg, int ratio)
+{
+    RowMap m;
+    m.base = 0;
+    m.seg = -1;
+    m.real = false;
+    m.first = true;
+    if (n_seg <= 0)
+        return m;
+    const int r0 = __ldg(cc), r1 = __ldg(cc + n_seg);
+    if (r < r0 || r >= r1)
+        return m;
+    const int s = find_segment(cc, n_seg, r);
+    const int b = r - __ldg(cc + s);
+    m.base = (int64_t)__ldg(cu + s) + (int64_t)b * ratio;
+    m.seg = s;
+    m.real = true;
+    m.first = (b == 0);
+    return m;
+}
+
+// 16-byte streaming load (read once: evict-first in L1 and L2).
+__device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
+
+}  // namespace csa
