@@ -133,6 +133,17 @@ CSA_API const char *csa_status_string(int status);
 /* Thread-local text of the calling thread's last non-OK return ("" if none). */
 CSA_API const char *csa_last_error_message(void);
 
+/*
+ * Device-side status of the current device, for diagnostics.  Kernels that wait
+ * on shared-memory barriers (the bulk-copy pipelines) bound every wait in time;
+ * on expiry they record a code in a per-device status word, stop, and exit
+ * normally, so that a wait that can never complete gives an error instead of a
+ * hung GPU.  This call SYNCHRONISES with the device (it reads the word back),
+ * returns CSA_OK if no kernel recorded anything and CSA_ERR_DEVICE_TIMEOUT
+ * otherwise; clear != 0 resets the word.  Not meant for the hot path.
+ */
+CSA_API int csa_device_status(int clear);
+
 /* Library version as an integer: major * 10000 + minor * 100 + patch. */
 CSA_API int csa_version(void);
 

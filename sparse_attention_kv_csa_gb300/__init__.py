@@ -30,7 +30,7 @@ from . import _build
 
 __all__ = [
     "csa_compress_fwd", "csa_compress_bwd", "csa_check_support", "csa_status_string",
-    "csa_last_error_message", "csa_version", "CSAError", "compress_forward", "compress_backward",
+    "csa_last_error_message", "csa_version", "csa_device_status", "CSAError", "compress_forward", "compress_backward",
     "library_path", "STATUS",
 ]
 
@@ -54,11 +54,12 @@ def _load():
     lib.csa_compress_fwd.argtypes = common + [P, P]
     lib.csa_compress_bwd.argtypes = common + [i64, P, P, P, P, P]
     lib.csa_check_support.argtypes = [i32, i32, i32, i64, i32]
+    lib.csa_device_status.argtypes = [ctypes.c_int]
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_last_error_message.argtypes = []
     lib.csa_last_error_message.restype = ctypes.c_char_p
-    for f in ("csa_compress_fwd", "csa_compress_bwd", "csa_check_support", "csa_version"):
+    for f in ("csa_compress_fwd", "csa_compress_bwd", "csa_check_support", "csa_version", "csa_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -102,6 +103,11 @@ def csa_last_error_message() -> str:
 
 def csa_version() -> int:
     return _lib.csa_version()
+
+
+def csa_device_status(clear: bool = False) -> int:
+    """Synchronises and returns the device status (0 = no bounded wait expired)."""
+    return _lib.csa_device_status(1 if clear else 0)
 
 
 def csa_check_support(ratio, coff, head_dim, n_tokens, capacity) -> int:

@@ -44,6 +44,7 @@ struct DeviceState {
     cudaError_t init_err = cudaSuccess;
     int num_sms = 0;
     cudaMemPool_t pool = nullptr;
+    unsigned *status = nullptr;  // device status word written by bounded waits
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -72,6 +73,10 @@ cudaError_t device_state(DeviceState **out)
                 uint64_t keep = 256ull << 20;
                 err = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
             }
+            if (err == cudaSuccess)
+                err = cudaMalloc(reinterpret_cast<void **>(&d.status), 256);
+            if (err == cudaSuccess)
+                err = cudaMemset(d.status, 0, 256);
         }
         d.init_err = err;
     });
@@ -177,9 +182,17 @@ int csa_compress_fwd(const void *kv, const void *score, const float *ape, const 
     CSA_TRY(check_ptr(score, "score", 16));
     CSA_TRY(check_ptr(ape, "ape", 16));
     CSA_TRY(check_ptr(out, "out", 16));
+    DeviceState *ds = nullptr;
+    cudaError_t e = device_state(&ds);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device set-up");
     csa::FwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim, capacity, out};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = csa::launch_fwd_small(p, st);
+    if (csa::stream_supported(ratio, coff, head_dim))
+        e = csa::launch_fwd_stream(p, csa::plan_stream(false, ratio, coff, head_dim, capacity, ds->num_sms),
+                                   ds->status, st);
+    else
+        e = csa::launch_fwd_small(p, ds->num_sms, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "forward launch");
     return CSA_OK;
@@ -213,17 +226,41 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
+    const bool streamed = csa::stream_supported(ratio, coff, head_dim);
+    const csa::StreamPlan sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, ds->num_sms);
     const csa::SmallBwdPlan pl = csa::plan_bwd_small(ratio, coff, head_dim, capacity, ds->num_sms);
+    const int64_t floats = streamed ? (int64_t)csa::stream_bwd_partials(sp, capacity) * ratio * coff * head_dim
+                                    : pl.partial_floats;
     void *partial = nullptr;
-    e = cudaMallocFromPoolAsync(&partial, (size_t)pl.partial_floats * sizeof(float), ds->pool, st);
+    e = cudaMallocFromPoolAsync(&partial, (size_t)floats * sizeof(float), ds->pool, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward workspace");
-    e = csa::launch_bwd_small(p, pl, static_cast<float *>(partial), st);
+    if (streamed)
+        e = csa::launch_bwd_stream(p, sp, static_cast<float *>(partial), ds->status, st);
+    else
+        e = csa::launch_bwd_small(p, pl, static_cast<float *>(partial), st);
     cudaError_t e2 = cudaFreeAsync(partial, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward launch");
     if (e2 != cudaSuccess)
         return cuda_fail(e2, "backward workspace release");
+    return CSA_OK;
+}
+
+int csa_device_status(int clear)
+{
+    DeviceState *ds = nullptr;
+    cudaError_t e = device_state(&ds);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device set-up");
+    unsigned word = 0;
+    e = cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear)
+        e = cudaMemset(ds->status, 0, sizeof(word));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "status read");
+    if (word != 0)
+        return fail(CSA_ERR_DEVICE_TIMEOUT, "a kernel recorded device status %u (bounded wait expired)", word);
     return CSA_OK;
 }
 

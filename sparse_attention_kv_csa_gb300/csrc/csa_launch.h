@@ -41,16 +41,41 @@ struct BwdParams {
 
 // Small-ratio family (window in registers).
 struct SmallBwdPlan {
-    int threads_x;       // threads along the columns (8 columns each), <= 64
+    int threads_x;       // threads along the columns (4 columns each)
     int col_slices;      // blocks along the columns (gridDim.y)
     int lanes;           // rows processed side by side in a block
-    int blocks;          // = number of grad_ape partials
+    int cluster;         // blocks per thread-block cluster (partials merged in DSMEM)
+    int blocks;          // gridDim.x, a multiple of cluster
+    int partials;        // grad_ape partials = blocks / cluster
     int rows_per_block;  // contiguous output rows per block
-    size_t smem;         // bytes of dynamic shared memory (lane merge)
+    size_t smem;         // bytes of dynamic shared memory (lane and cluster merge)
     int64_t partial_floats;
 };
 
-cudaError_t launch_fwd_small(const FwdParams &p, cudaStream_t st);
+cudaError_t launch_fwd_small(const FwdParams &p, int num_sms, cudaStream_t st);
+
+// grad_ape = fixed-order sum of n_partials partials of n floats each.
+cudaError_t launch_dape_finalize(const float *partial, int n_partials, int64_t n, float *dape, cudaStream_t st);
+
+// Streamed family (bulk-copy pipeline through shared memory), head_dim % 128 == 0.
+struct StreamPlan {
+    int tc;              // columns per thread block tile (consumer threads x 4)
+    int tiles;           // head_dim / tc (gridDim.y)
+    int threads;         // consumer warps + one producer warp, x 32
+    int stage_bytes;     // bytes per ring stage
+    int stages;          // ring depth
+    size_t red_bytes;    // backward: grad_ape staging in shared memory
+    size_t smem;         // dynamic shared memory per block
+    int cluster;         // backward: blocks per cluster
+    int num_sms;
+};
+
+bool stream_supported(int ratio, int coff, int head_dim);
+StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity, int num_sms);
+int stream_bwd_partials(const StreamPlan &pl, int capacity);
+cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st);
+cudaError_t launch_bwd_stream(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
+                              cudaStream_t st);
 SmallBwdPlan plan_bwd_small(int ratio, int coff, int head_dim, int capacity, int num_sms);
 cudaError_t launch_bwd_small(const BwdParams &p, const SmallBwdPlan &pl, float *partial, cudaStream_t st);
 

@@ -7,9 +7,12 @@
 //   head_dim + j with APE row k - ratio.  coff == 1: the own block only.
 //   out[b, j] = sum_k kv * softmax_k(score + ape), fp32, one final bf16 rounding.
 //
-// Work split: one thread owns 8 consecutive output columns j of one row, so
-// every window row it touches is one 16-byte vector of kv and one of score.  The
-// 8 columns are processed as 4 fp32 pairs with the packed .f32x2 instructions.
+// Work split: a thread owns a group of 2*NW consecutive output columns of one row
+// (NW 32-bit words of bf16 per window row and array, one 8- or 16-byte vector
+// load each).  Columns
+// are processed as fp32 pairs with the packed .f32x2 instructions.  Both kernels
+// are persistent and keep the next unit's window loads in flight (a second
+// register buffer) while the current unit is computed.
 //
 // Operation order (the same in the forward and in the backward's recompute;
 // invalid positions are skipped, valid ones taken in ascending k):
@@ -19,8 +22,12 @@
 // Backward, per valid k, with g = grad_out:
 //   go = g*o;  p = e_k*inv;  grad_kv = bf16(g*p);  ds = p*(g*kv - go);
 //   grad_score = bf16(ds);  ds is summed into this thread's grad_ape partial.
+#include <cooperative_groups.h>
+
 #include "csa_device.cuh"
 #include "csa_launch.h"
+
+namespace cg = cooperative_groups;
 
 namespace csa {
 
@@ -37,23 +44,77 @@ struct SmallArgs {
     int capacity;
 };
 
-// Window position k of a row: token and packed column of its 8-column group j.
+// ------------------------------------------------------------ vectors
+
+template <int NW>
+__device__ __forceinline__ void ld_words(uint32_t (&w)[NW], const uint16_t *p)
+{
+    if constexpr (NW == 4) {
+        const uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p));
+        w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+    } else if constexpr (NW == 2) {
+        const uint2 v = __ldcs(reinterpret_cast<const uint2 *>(p));
+        w[0] = v.x, w[1] = v.y;
+    } else {
+        static_assert(NW == 1, "NW is 1, 2 or 4");
+        w[0] = __ldcs(reinterpret_cast<const unsigned int *>(p));
+    }
+}
+
+template <int NW>
+__device__ __forceinline__ void st_words(uint16_t *p, const uint32_t (&w)[NW])
+{
+    if constexpr (NW == 4)
+        *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    else if constexpr (NW == 2)
+        *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+    else
+        *reinterpret_cast<uint32_t *>(p) = w[0];
+}
+
+template <int NW>
+__device__ __forceinline__ void st_zero(uint16_t *p)
+{
+    if constexpr (NW == 4)
+        *reinterpret_cast<uint4 *>(p) = make_uint4(0u, 0u, 0u, 0u);
+    else if constexpr (NW == 2)
+        *reinterpret_cast<uint2 *>(p) = make_uint2(0u, 0u);
+    else
+        *reinterpret_cast<uint32_t *>(p) = 0u;
+}
+
+// NW fp32 pairs of APE (read through the read-only cache; the table is small).
+template <int NW>
+__device__ __forceinline__ void ld_ape(float2 (&a)[NW], const float *p)
+{
+    if constexpr (NW == 1) {
+        a[0] = __ldg(reinterpret_cast<const float2 *>(p));
+    } else {
+#pragma unroll
+        for (int h = 0; h < NW / 2; ++h) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(p) + h);
+            a[2 * h] = make_float2(v.x, v.y);
+            a[2 * h + 1] = make_float2(v.z, v.w);
+        }
+    }
+}
+
+// ------------------------------------------------------------- window
+
+// Window position k of a row: token and packed column for column group j.
 template <int RATIO, int COFF>
 __device__ __forceinline__ void window_slot(int k, const RowMap &rm, int j, int head_dim,
-                                            int64_t &tok, int &col, int &arow)
+                                            int64_t &tok, int &col)
 {
     if (COFF == 2 && k < RATIO) {
         tok = rm.base - RATIO + k;
         col = j;
-        arow = k;
     } else if (COFF == 2) {
         tok = rm.base + (k - RATIO);
         col = head_dim + j;
-        arow = k - RATIO;
     } else {
         tok = rm.base + k;
         col = j;
-        arow = k;
     }
 }
 
@@ -73,166 +134,326 @@ __device__ __forceinline__ void ape_slot(int k, int j, int head_dim, int &arow, 
     }
 }
 
-// Loads the window of (row, 8 columns) and runs the pooling up to den/num.
-// On return: e[k][q] holds e_k for column pair q (valid k only), num/den per pair,
-// kvv[k] holds the raw kv vector.
 template <int RATIO, int COFF>
+__device__ __forceinline__ bool slot_valid(int k, const RowMap &rm)
+{
+    return !(COFF == 2 && k < RATIO && rm.first);
+}
+
+template <int RATIO, int COFF, int NW>
+struct Window {
+    uint32_t kv[COFF * RATIO][NW];
+    uint32_t sc[COFF * RATIO][NW];
+};
+
+template <int RATIO, int COFF, int NW>
+__device__ __forceinline__ void load_window(const SmallArgs &a, const RowMap &rm, int j,
+                                            Window<RATIO, COFF, NW> &w)
+{
+    const int64_t C = (int64_t)COFF * a.head_dim;
+#pragma unroll
+    for (int k = 0; k < COFF * RATIO; ++k) {
+        if (!slot_valid<RATIO, COFF>(k, rm))
+            continue;
+        int64_t tok;
+        int col;
+        window_slot<RATIO, COFF>(k, rm, j, a.head_dim, tok, col);
+        ld_words<NW>(w.kv[k], a.kv + tok * C + col);
+        ld_words<NW>(w.sc[k], a.score + tok * C + col);
+    }
+}
+
+// The softmax pooling of one (row, column group) up to den and num; e[k] holds e_k
+// for the valid positions.
+template <int RATIO, int COFF, int NW>
 __device__ __forceinline__ void pool_window(const SmallArgs &a, const RowMap &rm, int j,
-                                            uint4 (&kvv)[COFF * RATIO], float2 (&e)[COFF * RATIO][4],
-                                            float2 (&den)[4], float2 (&num)[4])
+                                            const Window<RATIO, COFF, NW> &w,
+                                            float2 (&e)[COFF * RATIO][NW], float2 (&den)[NW],
+                                            float2 (&num)[NW])
 {
     constexpr int W = COFF * RATIO;
     const int64_t C = (int64_t)COFF * a.head_dim;
-    const bool has_prev = (COFF == 2) && !rm.first;
-    uint4 scv[W];
+    float2 m[NW];
+#pragma unroll
+    for (int q = 0; q < NW; ++q)
+        m[q] = make_float2(-INFINITY, -INFINITY);
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-        if (COFF == 2 && k < RATIO && !has_prev)
+        if (!slot_valid<RATIO, COFF>(k, rm))
             continue;
-        int64_t tok;
-        int col, arow;
-        window_slot<RATIO, COFF>(k, rm, j, a.head_dim, tok, col, arow);
-        kvv[k] = ld_stream(a.kv + tok * C + col);
-        scv[k] = ld_stream(a.score + tok * C + col);
-    }
-    float m[8];
+        int arow, col;
+        ape_slot<RATIO, COFF>(k, j, a.head_dim, arow, col);
+        float2 ap[NW];
+        ld_ape<NW>(ap, a.ape + (int64_t)arow * C + col);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        m[i] = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < W; ++k) {
-        if (COFF == 2 && k < RATIO && !has_prev)
-            continue;
-        int64_t tok;
-        int col, arow;
-        window_slot<RATIO, COFF>(k, rm, j, a.head_dim, tok, col, arow);
-        const float4 *ap = reinterpret_cast<const float4 *>(a.ape + (int64_t)arow * C + col);
-        const float4 a0 = __ldg(ap), a1 = __ldg(ap + 1);
-        e[k][0] = add2(bf16x2_to_f2(scv[k].x), make_float2(a0.x, a0.y));
-        e[k][1] = add2(bf16x2_to_f2(scv[k].y), make_float2(a0.z, a0.w));
-        e[k][2] = add2(bf16x2_to_f2(scv[k].z), make_float2(a1.x, a1.y));
-        e[k][3] = add2(bf16x2_to_f2(scv[k].w), make_float2(a1.z, a1.w));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            m[2 * q] = max_nan(m[2 * q], e[k][q].x);
-            m[2 * q + 1] = max_nan(m[2 * q + 1], e[k][q].y);
+        for (int q = 0; q < NW; ++q) {
+            e[k][q] = add2(bf16x2_to_f2(w.sc[k][q]), ap[q]);
+            m[q].x = max_nan(m[q].x, e[k][q].x);
+            m[q].y = max_nan(m[q].y, e[k][q].y);
         }
     }
-    float2 negm[4];
+    float2 negm[NW];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        negm[q] = make_float2(-m[2 * q], -m[2 * q + 1]);
+    for (int q = 0; q < NW; ++q) {
+        negm[q] = make_float2(-m[q].x, -m[q].y);
         den[q] = make_float2(0.0f, 0.0f);
         num[q] = make_float2(0.0f, 0.0f);
     }
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-        if (COFF == 2 && k < RATIO && !has_prev)
+        if (!slot_valid<RATIO, COFF>(k, rm))
             continue;
-        const uint32_t kw[4] = {kvv[k].x, kvv[k].y, kvv[k].z, kvv[k].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < NW; ++q) {
             const float2 ek = exp2lanes(add2(e[k][q], negm[q]));
             e[k][q] = ek;
             den[q] = add2(den[q], ek);
-            num[q] = fma2(ek, bf16x2_to_f2(kw[q]), num[q]);
+            num[q] = fma2(ek, bf16x2_to_f2(w.kv[k][q]), num[q]);
+        }
+    }
+}
+
+// -------------------------------------------------------------- forward
+
+// Tile choices (compile-time): words of bf16 per window row per thread and the
+// minimum resident blocks per SM the register budget is sized for.
+#ifndef CSA_FWD_NW
+#define CSA_FWD_NW 2
+#endif
+#ifndef CSA_FWD_MINB
+#define CSA_FWD_MINB 3
+#endif
+constexpr int kFwdNW = CSA_FWD_NW;
+constexpr int kFwdThreads = 128;
+
+template <int RATIO, int COFF>
+struct FwdUnit {
+    Window<RATIO, COFF, kFwdNW> w;
+    RowMap rm;
+    int r, j;
+};
+
+template <int RATIO, int COFF>
+__device__ __forceinline__ void fwd_fetch(const SmallArgs &a, int u, int groups, FwdUnit<RATIO, COFF> &f)
+{
+    f.r = u / groups;
+    f.j = (u - f.r * groups) * (2 * kFwdNW);
+    f.rm = map_row(f.r, a.cu, a.cc, a.n_seg, RATIO);
+    load_window<RATIO, COFF, kFwdNW>(a, f.rm, f.j, f.w);
+}
+
+template <int RATIO, int COFF>
+__device__ __forceinline__ void fwd_compute(const SmallArgs &a, const FwdUnit<RATIO, COFF> &f,
+                                            uint16_t *__restrict__ out)
+{
+    constexpr int NW = kFwdNW;
+    float2 e[COFF * RATIO][NW], den[NW], num[NW];
+    pool_window<RATIO, COFF, NW>(a, f.rm, f.j, f.w, e, den, num);
+    uint32_t o[NW];
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+        const float2 inv = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
+        o[q] = f2_to_bf16x2(mul2(num[q], inv));
+    }
+    st_words<NW>(out + (int64_t)f.r * a.head_dim + f.j, o);
+}
+
+// Persistent: thread t takes units t, t + stride, ... (unit = row x column group,
+// consecutive threads on consecutive column groups, so loads coalesce).  Two unit
+// buffers alternate: the next unit's loads are issued before the current one is
+// computed.
+template <int RATIO, int COFF>
+__global__ void __launch_bounds__(kFwdThreads, CSA_FWD_MINB) fwd_small_kernel(SmallArgs a, uint16_t *__restrict__ out)
+{
+    const int groups = a.head_dim / (2 * kFwdNW);
+    const int total = a.capacity * groups;
+    const int stride = gridDim.x * blockDim.x;
+    int u = blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= total)
+        return;
+    FwdUnit<RATIO, COFF> A, B;
+    fwd_fetch<RATIO, COFF>(a, u, groups, A);
+    for (;;) {
+        int un = u + stride;
+        if (un < total)
+            fwd_fetch<RATIO, COFF>(a, un, groups, B);
+        fwd_compute<RATIO, COFF>(a, A, out);
+        if (un >= total)
+            break;
+        u = un;
+        un = u + stride;
+        if (un < total)
+            fwd_fetch<RATIO, COFF>(a, un, groups, A);
+        fwd_compute<RATIO, COFF>(a, B, out);
+        if (un >= total)
+            break;
+        u = un;
+    }
+}
+
+// ------------------------------------------------------------- backward
+
+#ifndef CSA_BWD_NW
+#define CSA_BWD_NW 2
+#endif
+#ifndef CSA_BWD_MINB
+#define CSA_BWD_MINB 3
+#endif
+#ifndef CSA_BWD_CLUSTER
+#define CSA_BWD_CLUSTER 4
+#endif
+constexpr int kBwdNW = CSA_BWD_NW;
+constexpr int kBwdThreads = 128;
+
+template <int RATIO, int COFF>
+struct BwdRow {
+    Window<RATIO, COFF, kBwdNW> w;
+    uint32_t g[kBwdNW];
+    RowMap rm;
+};
+
+template <int RATIO, int COFF>
+__device__ __forceinline__ void bwd_fetch(const SmallArgs &a, int r, int j, const uint16_t *__restrict__ grad_out,
+                                          BwdRow<RATIO, COFF> &f)
+{
+    f.rm = map_row(r, a.cu, a.cc, a.n_seg, RATIO);
+    if (!f.rm.real)
+        return;
+    load_window<RATIO, COFF, kBwdNW>(a, f.rm, j, f.w);
+    ld_words<kBwdNW>(f.g, grad_out + (int64_t)r * a.head_dim + j);
+}
+
+struct BwdOut {
+    uint16_t *dkv;
+    uint16_t *dscore;
+    int64_t n_tokens;
+};
+
+// Zero the gradient slots of tokens [t0, t1) in this thread's columns.
+template <int COFF>
+__device__ __forceinline__ void zero_tokens(const BwdOut &o, int64_t C, int head_dim, int j, int64_t t0,
+                                            int64_t t1)
+{
+    t1 = t1 < o.n_tokens ? t1 : o.n_tokens;
+    for (int64_t t = t0 < 0 ? 0 : t0; t < t1; ++t) {
+        st_zero<kBwdNW>(o.dkv + t * C + j);
+        st_zero<kBwdNW>(o.dscore + t * C + j);
+        if (COFF == 2) {
+            st_zero<kBwdNW>(o.dkv + t * C + head_dim + j);
+            st_zero<kBwdNW>(o.dscore + t * C + head_dim + j);
         }
     }
 }
 
 template <int RATIO, int COFF>
-__global__ void __launch_bounds__(256) fwd_small_kernel(SmallArgs a, uint16_t *__restrict__ out)
+__device__ __forceinline__ void bwd_compute(const SmallArgs &a, const BwdRow<RATIO, COFF> &f, int r, int j,
+                                            int R, const BwdOut &o, float2 (&acc)[COFF * RATIO][kBwdNW])
 {
     constexpr int W = COFF * RATIO;
-    const int groups = a.head_dim >> 3;
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= (int64_t)a.capacity * groups)
+    constexpr int NW = kBwdNW;
+    if (!f.rm.real)
         return;
-    const int r = (int)(t / groups);
-    const int j = (int)(t - (int64_t)r * groups) * 8;
-    const RowMap rm = map_row(r, a.cu, a.cc, a.n_seg, RATIO);
-
-    uint4 kvv[W];
-    float2 e[W][4], den[4], num[4];
-    pool_window<RATIO, COFF>(a, rm, j, kvv, e, den, num);
-
-    uint4 o;
-    uint32_t ow[4];
+    const int64_t C = (int64_t)COFF * a.head_dim;
+    float2 e[W][NW], den[NW], num[NW];
+    pool_window<RATIO, COFF, NW>(a, f.rm, j, f.w, e, den, num);
+    float2 g[NW], inv[NW], ngo[NW];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 inv = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
-        ow[q] = f2_to_bf16x2(mul2(num[q], inv));
+    for (int q = 0; q < NW; ++q) {
+        g[q] = bf16x2_to_f2(f.g[q]);
+        inv[q] = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
+        const float2 go = mul2(g[q], mul2(num[q], inv[q]));
+        ngo[q] = make_float2(-go.x, -go.y);
     }
-    o.x = ow[0];
-    o.y = ow[1];
-    o.z = ow[2];
-    o.w = ow[3];
-    *reinterpret_cast<uint4 *>(out + (int64_t)r * a.head_dim + j) = o;
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        if (!slot_valid<RATIO, COFF>(k, f.rm))
+            continue;
+        int64_t tok;
+        int col;
+        window_slot<RATIO, COFF>(k, f.rm, j, a.head_dim, tok, col);
+        uint32_t dk[NW], dsw[NW];
+#pragma unroll
+        for (int q = 0; q < NW; ++q) {
+            const float2 p = mul2(e[k][q], inv[q]);
+            dk[q] = f2_to_bf16x2(mul2(g[q], p));
+            const float2 ds = mul2(p, add2(mul2(g[q], bf16x2_to_f2(f.w.kv[k][q])), ngo[q]));
+            dsw[q] = f2_to_bf16x2(ds);
+            acc[k][q] = add2(acc[k][q], ds);
+        }
+        if (tok < o.n_tokens) {
+            st_words<NW>(o.dkv + tok * C + col, dk);
+            st_words<NW>(o.dscore + tok * C + col, dsw);
+        }
+    }
+    // Last block of its segment: its own first-half columns are read by no row
+    // (coff 2), and the tokens up to the next real block form a gap.
+    if (r + 1 == __ldg(a.cc + f.rm.seg + 1)) {
+        if (COFF == 2) {
+            for (int i = 0; i < RATIO; ++i) {
+                const int64_t tok = f.rm.base + i;
+                if (tok < o.n_tokens) {
+                    st_zero<NW>(o.dkv + tok * C + j);
+                    st_zero<NW>(o.dscore + tok * C + j);
+                }
+            }
+        }
+        int64_t next = o.n_tokens;
+        if (r + 1 < R)
+            next = map_row(r + 1, a.cu, a.cc, a.n_seg, RATIO).base;
+        zero_tokens<COFF>(o, C, a.head_dim, j, f.rm.base + RATIO, next);
+    }
 }
 
-// Backward.  Block = (up to 64 threads along x, 8 columns each) x (lanes along y);
-// blockIdx.y picks the block's slice of columns when head_dim > 512.  Block p owns
-// output rows [p*rows_per_block, ...) of the static capacity; lane y takes rows
-// y, y + lanes, ... of that range in ascending order.  Each thread keeps the
-// grad_ape sums of its 8 columns and all window positions in registers; at the
-// end the lanes are added in ascending lane order through shared memory and the
-// block writes one [ratio, coff*head_dim] partial.  dape_finalize_kernel then adds
-// the partials in ascending block order: no atomics, a fixed order, so grad_ape is
-// bitwise reproducible run to run.
+// Backward.  Block = (threads_x column groups of 4 columns) x (lanes); blockIdx.y
+// picks a slice of columns for wide heads.  Block b owns output rows
+// [b*rows_per_block, (b+1)*rows_per_block) of the static capacity; lane y takes rows
+// y, y + lanes, ... of that range in ascending order, prefetching its next row.
+// Each thread keeps the grad_ape sums of its columns and window positions in
+// registers.  At the end the lanes are added in ascending lane order in shared
+// memory; then the blocks of a thread-block cluster add their shared-memory
+// partials in ascending cluster rank through distributed shared memory and the
+// cluster writes one [ratio, coff*head_dim] partial.  dape_finalize_kernel adds the
+// partials in a fixed order.  No atomics, fixed orders: grad_ape is bitwise
+// reproducible run to run.
 //
 // Gradient coverage ("CSA Fused Compressor", Class API: every never-consumed slot
 // gets an exact zero from one owner).  A real row writes the slots it reads; the
 // last block of a segment also zeroes its own first-half columns (coff == 2) and
 // the gap of tokens after its block up to the next real row's block (or up to
 // n_tokens): the segment's tail, segments shorter than ratio, token padding.  The
-// thread group of row 0 zeroes the tokens before the first real block.  Every
-// token of [0, n_tokens) is thus written exactly once.
+// threads of row 0 zero the tokens before the first real block.  Every token of
+// [0, n_tokens) is thus written exactly once.
 template <int RATIO, int COFF>
-__global__ void __launch_bounds__(256) bwd_small_kernel(SmallArgs a, int rows_per_block,
-                                                        int64_t n_tokens_arg,
-                                                        const uint16_t *__restrict__ grad_out,
-                                                        uint16_t *__restrict__ dkv,
-                                                        uint16_t *__restrict__ dscore,
-                                                        float *__restrict__ partial)
+__global__ void __launch_bounds__(kBwdThreads, CSA_BWD_MINB)
+    bwd_small_kernel(SmallArgs a, int rows_per_block, int64_t n_tokens_arg,
+                     const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
+                     uint16_t *__restrict__ dscore, float *__restrict__ partial)
 {
     constexpr int W = COFF * RATIO;
+    constexpr int NW = kBwdNW;
     extern __shared__ float red[];
     const int lanes = blockDim.y;
     const int x = threadIdx.x, y = threadIdx.y;
-    const int j = (blockIdx.y * blockDim.x + x) * 8;
+    const int j = (blockIdx.y * blockDim.x + x) * (2 * NW);
     const bool col_ok = j < a.head_dim;  // the last column slice may be partial
     const int64_t C = (int64_t)COFF * a.head_dim;
-    const int64_t n_tokens = n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg);
+    BwdOut o{dkv, dscore, n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg)};
     const int R = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;
     const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
-    const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
-
-    // Zero the gradient slots of tokens [t0, t1) in this thread's columns.
-    auto zero_tokens = [&](int64_t t0, int64_t t1) {
-        t1 = t1 < n_tokens ? t1 : n_tokens;
-        for (int64_t t = t0 < 0 ? 0 : t0; t < t1; ++t) {
-            *reinterpret_cast<uint4 *>(dkv + t * C + j) = zero4;
-            *reinterpret_cast<uint4 *>(dscore + t * C + j) = zero4;
-            if (COFF == 2) {
-                *reinterpret_cast<uint4 *>(dkv + t * C + a.head_dim + j) = zero4;
-                *reinterpret_cast<uint4 *>(dscore + t * C + a.head_dim + j) = zero4;
-            }
-        }
-    };
 
     // Leading gap: tokens before the first real block.
     if (blockIdx.x == 0 && y == 0 && col_ok) {
-        int64_t lead = n_tokens;
+        int64_t lead = o.n_tokens;
         if (R0 < R)
             lead = map_row(R0, a.cu, a.cc, a.n_seg, RATIO).base;  // a first block
-        zero_tokens(0, lead);
+        zero_tokens<COFF>(o, C, a.head_dim, j, 0, lead);
     }
 
-    float2 acc[W][4];
+    float2 acc[W][NW];
 #pragma unroll
     for (int k = 0; k < W; ++k)
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < NW; ++q)
             acc[k][q] = make_float2(0.0f, 0.0f);
 
     const int r_begin = blockIdx.x * rows_per_block;
@@ -241,96 +462,41 @@ __global__ void __launch_bounds__(256) bwd_small_kernel(SmallArgs a, int rows_pe
     r_end = r_end < R ? r_end : R;  // padding rows carry no gradient
     if (!col_ok)
         r_end = r_begin;
-    for (int r = r_begin + y; r < r_end; r += lanes) {
-        const RowMap rm = map_row(r, a.cu, a.cc, a.n_seg, RATIO);
-        if (!rm.real)
-            continue;
-        uint4 kvv[W];
-        float2 e[W][4], den[4], num[4];
-        pool_window<RATIO, COFF>(a, rm, j, kvv, e, den, num);
-
-        const uint4 gv = ld_stream(grad_out + (int64_t)r * a.head_dim + j);
-        const float2 g[4] = {bf16x2_to_f2(gv.x), bf16x2_to_f2(gv.y), bf16x2_to_f2(gv.z),
-                             bf16x2_to_f2(gv.w)};
-        float2 inv[4], go[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            inv[q] = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
-            go[q] = mul2(g[q], mul2(num[q], inv[q]));
-        }
-        const bool has_prev = (COFF == 2) && !rm.first;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-            if (COFF == 2 && k < RATIO && !has_prev)
-                continue;
-            int64_t tok;
-            int col, arow;
-            window_slot<RATIO, COFF>(k, rm, j, a.head_dim, tok, col, arow);
-            const uint32_t kw[4] = {kvv[k].x, kvv[k].y, kvv[k].z, kvv[k].w};
-            uint32_t dk[4], dsw[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 p = mul2(e[k][q], inv[q]);
-                dk[q] = f2_to_bf16x2(mul2(g[q], p));
-                const float2 gvk = mul2(g[q], bf16x2_to_f2(kw[q]));
-                const float2 ds = mul2(p, add2(gvk, make_float2(-go[q].x, -go[q].y)));
-                dsw[q] = f2_to_bf16x2(ds);
-                acc[k][q] = add2(acc[k][q], ds);
-            }
-            if (tok < n_tokens) {
-                *reinterpret_cast<uint4 *>(dkv + tok * C + col) = make_uint4(dk[0], dk[1], dk[2], dk[3]);
-                *reinterpret_cast<uint4 *>(dscore + tok * C + col) =
-                    make_uint4(dsw[0], dsw[1], dsw[2], dsw[3]);
-            }
-        }
-        // Last block of its segment: own first-half columns are never read (coff 2),
-        // and the tokens up to the next real block are a gap.
-        const bool last = (r + 1 == __ldg(a.cc + rm.seg + 1));
-        if (last) {
-            if (COFF == 2) {
-                for (int i = 0; i < RATIO; ++i) {
-                    const int64_t tok = rm.base + i;
-                    if (tok < n_tokens) {
-                        *reinterpret_cast<uint4 *>(dkv + tok * C + j) = zero4;
-                        *reinterpret_cast<uint4 *>(dscore + tok * C + j) = zero4;
-                    }
-                }
-            }
-            int64_t next = n_tokens;
-            if (r + 1 < R)
-                next = map_row(r + 1, a.cu, a.cc, a.n_seg, RATIO).base;
-            zero_tokens(rm.base + RATIO, next);
+    int r = r_begin + y;
+    if (r < r_end) {
+        BwdRow<RATIO, COFF> A, B;
+        bwd_fetch<RATIO, COFF>(a, r, j, grad_out, A);
+        for (;;) {
+            int rn = r + lanes;
+            if (rn < r_end)
+                bwd_fetch<RATIO, COFF>(a, rn, j, grad_out, B);
+            bwd_compute<RATIO, COFF>(a, A, r, j, R, o, acc);
+            if (rn >= r_end)
+                break;
+            r = rn;
+            rn = r + lanes;
+            if (rn < r_end)
+                bwd_fetch<RATIO, COFF>(a, rn, j, grad_out, A);
+            bwd_compute<RATIO, COFF>(a, B, r, j, R, o, acc);
+            if (rn >= r_end)
+                break;
+            r = rn;
         }
     }
 
-    // grad_ape partial of this block: lanes added in ascending order in shared
-    // memory laid out [ape row][half][slice column], then copied out.
-    float *dst = partial + (int64_t)blockIdx.x * RATIO * C;
-    if (lanes == 1) {
-        if (!col_ok)
-            return;
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-            int col, arow;
-            ape_slot<RATIO, COFF>(k, j, a.head_dim, arow, col);
-            float4 *d = reinterpret_cast<float4 *>(dst + (int64_t)arow * C + col);
-            d[0] = make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
-            d[1] = make_float4(acc[k][2].x, acc[k][2].y, acc[k][3].x, acc[k][3].y);
-        }
-        return;
-    }
-    const int SW = blockDim.x * 8;  // columns per half in this block's slice
+    // Lanes -> shared memory [ape row][half][slice column], ascending lane order.
+    const int SW = blockDim.x * 2 * NW;  // columns per half in this block's slice
     const int c0 = blockIdx.y * SW;
     for (int l = 0; l < lanes; ++l) {
         if (y == l && col_ok) {
 #pragma unroll
             for (int k = 0; k < W; ++k) {
-                int col, arow;
+                int arow, col;
                 ape_slot<RATIO, COFF>(k, j, a.head_dim, arow, col);
                 const int half = col >= a.head_dim ? 1 : 0;
                 float *sp = red + (arow * COFF + half) * SW + (j - c0);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < NW; ++q) {
                     if (l == 0) {
                         sp[2 * q] = acc[k][q].x;
                         sp[2 * q + 1] = acc[k][q].y;
@@ -343,95 +509,149 @@ __global__ void __launch_bounds__(256) bwd_small_kernel(SmallArgs a, int rows_pe
         }
         __syncthreads();
     }
-    const int nthreads = blockDim.x * blockDim.y;
+
+    // Cluster: block ranks' partials added in ascending rank order; each block of
+    // the cluster reduces and writes a share of the entries.
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int rank = (int)cluster.block_rank();
+    const int nrank = (int)cluster.num_blocks();
+    const int per_row4 = SW / 4;
+    const int n4 = RATIO * COFF * per_row4;
+    const int share = (n4 + nrank - 1) / nrank;
+    const int i_lo = rank * share;
+    const int i_hi = i_lo + share < n4 ? i_lo + share : n4;
+    float *dst = partial + (int64_t)(blockIdx.x / nrank) * RATIO * C;
     const int tid = y * blockDim.x + x;
-    const int per_row4 = SW / 4;  // float4 per (ape row, half)
-    for (int i = tid; i < RATIO * COFF * per_row4; i += nthreads) {
+    const int nthreads = blockDim.x * blockDim.y;
+    for (int i = i_lo + tid; i < i_hi; i += nthreads) {
         const int rh = i / per_row4, lc = (i - rh * per_row4) * 4;
         const int arow = rh / COFF, half = rh - arow * COFF;
-        if (c0 + lc < a.head_dim)
-            *reinterpret_cast<float4 *>(dst + (int64_t)arow * C + half * a.head_dim + c0 + lc) =
-                *reinterpret_cast<const float4 *>(red + rh * SW + lc);
+        if (c0 + lc >= a.head_dim)
+            continue;
+        float4 s = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(red, 0) + rh * SW + lc);
+        for (int q = 1; q < nrank; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(red, q) + rh * SW + lc);
+            s.x = __fadd_rn(s.x, v.x);
+            s.y = __fadd_rn(s.y, v.y);
+            s.z = __fadd_rn(s.z, v.z);
+            s.w = __fadd_rn(s.w, v.w);
+        }
+        *reinterpret_cast<float4 *>(dst + (int64_t)arow * C + half * a.head_dim + c0 + lc) = s;
     }
+    cluster.sync();  // keep this block's shared memory alive until all ranks read it
 }
 
 }  // namespace
 
-// grad_ape = sum of the partials in ascending order: ((p0 + p1) + p2) + ...
+// grad_ape = the partials summed in a fixed order.  Eight threads per 4-float
+// column: thread t adds partials [t*P/8, (t+1)*P/8) in ascending order, then the
+// eight subtotals are combined by a fixed butterfly ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)).
 __global__ void __launch_bounds__(256) dape_finalize_kernel(const float *__restrict__ partial,
                                                             int n_partials, int64_t n,
                                                             float *__restrict__ dape)
 {
-    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (4 * i >= n)
-        return;
-    const float4 *p = reinterpret_cast<const float4 *>(partial) + i;
+    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t i = gt >> 3;
+    const int t = (int)(gt & 7);
     const int64_t stride = n / 4;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    int b = 0;
-    constexpr int U = 16;
-    for (; b + U <= n_partials; b += U) {
-        float4 v[U];
+    if (i < stride) {
+        const int lo = (int)((int64_t)t * n_partials / 8), hi = (int)((int64_t)(t + 1) * n_partials / 8);
+        const float4 *p = reinterpret_cast<const float4 *>(partial) + i;
+        int b = lo;
+        for (; b + 4 <= hi; b += 4) {
+            float4 v[4];
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            v[u] = __ldcg(p + (int64_t)(b + u) * stride);
+            for (int u = 0; u < 4; ++u)
+                v[u] = __ldcg(p + (int64_t)(b + u) * stride);
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            acc.x = __fadd_rn(acc.x, v[u].x);
-            acc.y = __fadd_rn(acc.y, v[u].y);
-            acc.z = __fadd_rn(acc.z, v[u].z);
-            acc.w = __fadd_rn(acc.w, v[u].w);
+            for (int u = 0; u < 4; ++u) {
+                acc.x = __fadd_rn(acc.x, v[u].x);
+                acc.y = __fadd_rn(acc.y, v[u].y);
+                acc.z = __fadd_rn(acc.z, v[u].z);
+                acc.w = __fadd_rn(acc.w, v[u].w);
+            }
+        }
+        for (; b < hi; ++b) {
+            const float4 v = __ldcg(p + (int64_t)b * stride);
+            acc.x = __fadd_rn(acc.x, v.x);
+            acc.y = __fadd_rn(acc.y, v.y);
+            acc.z = __fadd_rn(acc.z, v.z);
+            acc.w = __fadd_rn(acc.w, v.w);
         }
     }
-    for (; b < n_partials; ++b) {
-        const float4 v = __ldcg(p + (int64_t)b * stride);
-        acc.x = __fadd_rn(acc.x, v.x);
-        acc.y = __fadd_rn(acc.y, v.y);
-        acc.z = __fadd_rn(acc.z, v.z);
-        acc.w = __fadd_rn(acc.w, v.w);
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) {
+        acc.x = __fadd_rn(acc.x, __shfl_xor_sync(0xffffffffu, acc.x, m));
+        acc.y = __fadd_rn(acc.y, __shfl_xor_sync(0xffffffffu, acc.y, m));
+        acc.z = __fadd_rn(acc.z, __shfl_xor_sync(0xffffffffu, acc.z, m));
+        acc.w = __fadd_rn(acc.w, __shfl_xor_sync(0xffffffffu, acc.w, m));
     }
-    reinterpret_cast<float4 *>(dape)[i] = acc;
+    if (i < stride && t == 0)
+        reinterpret_cast<float4 *>(dape)[i] = acc;
 }
 
 // ------------------------------------------------------------ launchers
 
-template <int RATIO, int COFF>
-static cudaError_t launch_fwd_small_t(const FwdParams &p, cudaStream_t st)
+cudaError_t launch_dape_finalize(const float *partial, int n_partials, int64_t n, float *dape, cudaStream_t st)
 {
-    SmallArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
-                p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity};
-    const int64_t threads = (int64_t)p.capacity * (p.head_dim / 8);
-    const int block = 256;
-    const int64_t grid = (threads + block - 1) / block;
-    fwd_small_kernel<RATIO, COFF><<<(unsigned)grid, block, 0, st>>>(a, static_cast<uint16_t *>(p.out));
+    const int64_t threads = n / 4 * 8;
+    dape_finalize_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, n_partials, n, dape);
     return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_small(const FwdParams &p, cudaStream_t st)
+template <int RATIO, int COFF>
+static cudaError_t launch_fwd_small_t(const FwdParams &p, int num_sms, cudaStream_t st)
+{
+    SmallArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
+                p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity};
+    const int64_t units = (int64_t)p.capacity * (p.head_dim / (2 * kFwdNW));
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_small_kernel<RATIO, COFF>,
+                                                                  kFwdThreads, 0);
+    if (e != cudaSuccess)
+        return e;
+    int64_t grid = (units + kFwdThreads - 1) / kFwdThreads;
+    const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * num_sms;
+    if (grid > resident)
+        grid = resident;
+    fwd_small_kernel<RATIO, COFF><<<(unsigned)grid, kFwdThreads, 0, st>>>(a, static_cast<uint16_t *>(p.out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_small(const FwdParams &p, int num_sms, cudaStream_t st)
 {
     if (p.ratio == 4 && p.coff == 2)
-        return launch_fwd_small_t<4, 2>(p, st);
+        return launch_fwd_small_t<4, 2>(p, num_sms, st);
     if (p.ratio == 4 && p.coff == 1)
-        return launch_fwd_small_t<4, 1>(p, st);
+        return launch_fwd_small_t<4, 1>(p, num_sms, st);
     return cudaErrorInvalidValue;
 }
 
 SmallBwdPlan plan_bwd_small(int ratio, int coff, int head_dim, int capacity, int num_sms)
 {
     SmallBwdPlan pl;
-    const int groups = head_dim / 8;
-    pl.threads_x = groups < 64 ? groups : 64;
+    const int groups = head_dim / (2 * kBwdNW);
+    pl.threads_x = groups < kBwdThreads ? groups : kBwdThreads;
     pl.col_slices = (groups + pl.threads_x - 1) / pl.threads_x;
-    pl.lanes = 128 / pl.threads_x > 1 ? 128 / pl.threads_x : 1;
-    const int max_blocks = (num_sms * 2 + pl.col_slices - 1) / pl.col_slices;
+    pl.lanes = kBwdThreads / pl.threads_x > 1 ? kBwdThreads / pl.threads_x : 1;
+    pl.cluster = CSA_BWD_CLUSTER;
+    const int resident = CSA_BWD_MINB * num_sms;  // blocks the register budget is sized for
+    int max_blocks = resident / pl.col_slices;
+    max_blocks = max_blocks / pl.cluster * pl.cluster;
+    if (max_blocks < pl.cluster)
+        max_blocks = pl.cluster;
     const int rows = capacity > 0 ? capacity : 1;
     int blocks = (rows + pl.lanes - 1) / pl.lanes;
     if (blocks > max_blocks)
         blocks = max_blocks;
     pl.rows_per_block = (rows + blocks - 1) / blocks;
-    pl.blocks = (rows + pl.rows_per_block - 1) / pl.rows_per_block;
-    pl.smem = pl.lanes > 1 ? (size_t)ratio * coff * pl.threads_x * 8 * sizeof(float) : 0;
-    pl.partial_floats = (int64_t)pl.blocks * ratio * coff * head_dim;
+    blocks = (rows + pl.rows_per_block - 1) / pl.rows_per_block;
+    pl.blocks = (blocks + pl.cluster - 1) / pl.cluster * pl.cluster;
+    pl.smem = (size_t)ratio * coff * pl.threads_x * 2 * kBwdNW * sizeof(float);
+    pl.partials = pl.blocks / pl.cluster;
+    pl.partial_floats = (int64_t)pl.partials * ratio * coff * head_dim;
     return pl;
 }
 
@@ -447,18 +667,26 @@ static cudaError_t launch_bwd_small_t(const BwdParams &p, const SmallBwdPlan &pl
         if (e != cudaSuccess)
             return e;
     }
-    dim3 block(pl.threads_x, pl.lanes);
-    dim3 grid(pl.blocks, pl.col_slices);
-    kern<<<grid, block, pl.smem, st>>>(a, pl.rows_per_block, p.n_tokens,
-                                           static_cast<const uint16_t *>(p.grad_out),
-                                           static_cast<uint16_t *>(p.dkv),
-                                           static_cast<uint16_t *>(p.dscore), partial);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.blocks, pl.col_slices, 1);
+    cfg.blockDim = dim3(pl.threads_x, pl.lanes, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, pl.rows_per_block, p.n_tokens,
+                                       static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
+                                       static_cast<uint16_t *>(p.dscore), partial);
     if (e != cudaSuccess)
         return e;
     const int64_t n = (int64_t)RATIO * COFF * p.head_dim;
-    const int64_t threads = n / 4;
-    dape_finalize_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, pl.blocks, n, p.dape);
+    const int64_t threads = n / 4 * 8;
+    dape_finalize_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, pl.partials, n, p.dape);
     return cudaGetLastError();
 }
 

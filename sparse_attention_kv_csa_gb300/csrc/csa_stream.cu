@@ -1,0 +1,590 @@
+// Streamed Compressor kernels for small ratios: a bulk-copy pipeline into shared
+// memory.  Used when head_dim is a multiple of 128.
+//
+// Semantics and operation order are exactly those of csa_small.cu ("CSA Fused
+// Compressor", cuDNN frontend docs, sections Semantics and Numerics): window
+// positions in ascending k, invalid ones skipped; s = score + ape; NaN-propagating
+// max; e = exp(s - m) with the library's exp; den and num accumulated in ascending
+// k; inv = rcp.rn(den); out = bf16(num * inv); backward p = e*inv,
+// grad_kv = bf16(g*p), ds = p*(g*kv - g*o).  Results are bitwise those of
+// csa_small.cu.
+//
+// Structure (per thread block, persistent over the rows b, b + gridDim.x, ...):
+//   * one producer warp: for each row, waits for a free stage of a shared-memory
+//     ring, then issues raw bulk copies (cp.async.bulk) of every window row the
+//     output row reads -- each (token, half) is one contiguous run of TC*2 bytes --
+//     and, in the backward, the grad_out row; completion is counted in bytes on the
+//     stage's "full" mbarrier;
+//   * consumer warps: thread t owns columns [c0 + 4t, c0 + 4t + 4) of the block's
+//     column tile for every row, so its APE values stay in registers; it waits on
+//     the stage's "full" barrier, computes from shared memory, writes its outputs
+//     and releases the stage on the "empty" barrier.
+// Every wait is bounded in time; on expiry a timeout is recorded in the status
+// word, the loops stop, copies still in flight are drained, and the kernel exits
+// normally (no trap, no hang).
+#include <cooperative_groups.h>
+
+#include "csa_device.cuh"
+#include "csa_launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace csa {
+
+namespace {
+
+struct StreamArgs {
+    const uint16_t *kv;
+    const uint16_t *score;
+    const float *ape;
+    const int32_t *cu;
+    const int32_t *cc;
+    int n_seg;
+    int head_dim;
+    int capacity;
+    int stages;        // ring depth
+    int stage_bytes;   // bytes per stage (multiple of 128)
+    unsigned *status;  // caller-visible status word
+};
+
+struct StageMeta {
+    int64_t base;
+    int seg;
+    int row;
+    int real;
+    int first;
+    int pad[2];
+};
+
+// Window position k reads part p = k / RATIO, token i = k % RATIO of the part.
+// coff 2: part 0 = the previous block on the first-half columns, part 1 = the own
+// block on the second-half columns; coff 1: part 0 = the own block.  The part's
+// tokens start at base + (p - (COFF - 1)) * RATIO and its columns at p * head_dim.
+template <int RATIO, int COFF>
+__host__ __device__ __forceinline__ int stage_offset(int arr, int part, int i, int tc)
+{
+    return ((arr * COFF + part) * RATIO + i) * tc * 2;
+}
+
+template <int RATIO, int COFF>
+__host__ __device__ __forceinline__ int window_bytes(int tc)
+{
+    return 2 * COFF * RATIO * tc * 2;
+}
+
+struct Smem {
+    unsigned char *stages;
+    StageMeta *meta;
+    uint64_t *full;
+    uint64_t *empty;
+    float *red;
+};
+
+__device__ __forceinline__ Smem carve(unsigned char *base, int stages, int stage_bytes)
+{
+    Smem s;
+    s.stages = base;
+    unsigned char *p = base + (size_t)stages * stage_bytes;
+    s.meta = reinterpret_cast<StageMeta *>(p);
+    p += sizeof(StageMeta) * stages;
+    s.full = reinterpret_cast<uint64_t *>(p);
+    s.empty = s.full + stages;
+    p = reinterpret_cast<unsigned char *>(s.empty + stages);
+    s.red = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
+    return s;
+}
+
+__host__ size_t smem_bytes(int stages, int stage_bytes, size_t red_bytes)
+{
+    return (size_t)stages * stage_bytes + (sizeof(StageMeta) + 16) * stages + 16 + red_bytes;
+}
+
+// ---------------------------------------------------------------- producer
+
+// Issues the copies of rows row0, row0 + rstride, ... < rend.  Runs on one lane.
+template <int RATIO, int COFF, bool BWD>
+__device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int row0, int rstride, int rend,
+                        const uint16_t *__restrict__ grad_out)
+{
+    const int64_t C = (int64_t)COFF * a.head_dim;
+    const uint32_t run = (uint32_t)tc * 2;
+    int issued = 0;
+    for (int it = 0;; ++it) {
+        const int row = row0 + it * rstride;
+        if (row >= rend)
+            break;
+        const int st = it % a.stages;
+        const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+        if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
+            break;
+        const RowMap rm = map_row(row, a.cu, a.cc, a.n_seg, RATIO);
+        StageMeta &m = s.meta[st];
+        m.base = rm.base;
+        m.seg = rm.seg;
+        m.row = row;
+        m.real = rm.real;
+        m.first = rm.first;
+        const bool load = BWD ? rm.real : true;
+        const int p0 = (COFF == 2 && rm.first) ? 1 : 0;
+        const uint32_t bytes = load ? (uint32_t)((COFF - p0) * 2 * RATIO) * run + (BWD ? run : 0u) : 0u;
+        const uint32_t fb = smem_addr(&s.full[st]);
+        mbar_arrive_expect_tx(fb, bytes);
+        if (load) {
+            const uint32_t dst = smem_addr(s.stages + (size_t)st * a.stage_bytes);
+            for (int p = p0; p < COFF; ++p) {
+                const int64_t tok0 = rm.base + (int64_t)(p - (COFF - 1)) * RATIO;
+                const int64_t col = (int64_t)p * a.head_dim + c0;
+#pragma unroll
+                for (int i = 0; i < RATIO; ++i) {
+                    const int64_t g = (tok0 + i) * C + col;
+                    bulk_g2s(dst + stage_offset<RATIO, COFF>(0, p, i, tc), a.kv + g, run, fb);
+                    bulk_g2s(dst + stage_offset<RATIO, COFF>(1, p, i, tc), a.score + g, run, fb);
+                }
+            }
+            if (BWD)
+                bulk_g2s(dst + window_bytes<RATIO, COFF>(tc), grad_out + (int64_t)row * a.head_dim + c0, run, fb);
+        }
+        issued = it + 1;
+    }
+    // Copies of the last (up to) `stages` rows may still be in flight if the
+    // consumers stopped early: wait for them before the block may exit.
+    const int lo = issued > a.stages ? issued - a.stages : 0;
+    for (int it = lo; it < issued; ++it)
+        mbar_wait(smem_addr(&s.full[it % a.stages]), (uint32_t)(it / a.stages) & 1u, a.status);
+}
+
+// ---------------------------------------------------------------- consumer
+
+template <int RATIO, int COFF>
+struct ApeRegs {
+    float2 v[COFF * RATIO][2];
+};
+
+template <int RATIO, int COFF>
+__device__ __forceinline__ void load_ape(const StreamArgs &a, int col0, ApeRegs<RATIO, COFF> &ap)
+{
+    const int64_t C = (int64_t)COFF * a.head_dim;
+#pragma unroll
+    for (int k = 0; k < COFF * RATIO; ++k) {
+        const int p = k / RATIO, i = k % RATIO;
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(a.ape + i * C + (int64_t)p * a.head_dim + col0));
+        ap.v[k][0] = make_float2(v.x, v.y);
+        ap.v[k][1] = make_float2(v.z, v.w);
+    }
+}
+
+// Reads the thread's two words (4 bf16) of window position k from the stage.
+template <int RATIO, int COFF>
+__device__ __forceinline__ uint2 stage_words(const unsigned char *stage, int arr, int k, int tc, int lc)
+{
+    const int p = k / RATIO, i = k % RATIO;
+    return *reinterpret_cast<const uint2 *>(stage + stage_offset<RATIO, COFF>(arr, p, i, tc) + lc * 2);
+}
+
+template <int RATIO, int COFF>
+__device__ __forceinline__ void pool_stage(const unsigned char *stage, int tc, int lc, bool first,
+                                           const ApeRegs<RATIO, COFF> &ap, uint2 (&kvw)[COFF * RATIO],
+                                           float2 (&e)[COFF * RATIO][2], float2 (&den)[2], float2 (&num)[2])
+{
+    constexpr int W = COFF * RATIO;
+    float2 m[2] = {make_float2(-INFINITY, -INFINITY), make_float2(-INFINITY, -INFINITY)};
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        if (COFF == 2 && k < RATIO && first)
+            continue;
+        const uint2 sw = stage_words<RATIO, COFF>(stage, 1, k, tc, lc);
+        kvw[k] = stage_words<RATIO, COFF>(stage, 0, k, tc, lc);
+        e[k][0] = add2(bf16x2_to_f2(sw.x), ap.v[k][0]);
+        e[k][1] = add2(bf16x2_to_f2(sw.y), ap.v[k][1]);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            m[q].x = max_nan(m[q].x, e[k][q].x);
+            m[q].y = max_nan(m[q].y, e[k][q].y);
+        }
+    }
+    float2 negm[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        negm[q] = make_float2(-m[q].x, -m[q].y);
+        den[q] = make_float2(0.0f, 0.0f);
+        num[q] = make_float2(0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        if (COFF == 2 && k < RATIO && first)
+            continue;
+        const uint32_t kw[2] = {kvw[k].x, kvw[k].y};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float2 ek = exp2lanes(add2(e[k][q], negm[q]));
+            e[k][q] = ek;
+            den[q] = add2(den[q], ek);
+            num[q] = fma2(ek, bf16x2_to_f2(kw[q]), num[q]);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- forward
+
+template <int RATIO, int COFF>
+__global__ void __launch_bounds__(160) fwd_stream_kernel(StreamArgs a, uint16_t *__restrict__ out)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int ncw = blockDim.x / 32 - 1;  // consumer warps; the last warp produces
+    const int tc = ncw * 128;
+    const int c0 = blockIdx.y * tc;
+    const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(smem_addr(&s.full[i]), 1);
+            mbar_init(smem_addr(&s.empty[i]), ncw);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (warp == ncw) {
+        if (lane == 0)
+            produce<RATIO, COFF, false>(a, s, tc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
+        return;
+    }
+    const int lc = threadIdx.x * 4;  // local column of this thread in the tile
+    ApeRegs<RATIO, COFF> ap;
+    load_ape<RATIO, COFF>(a, c0 + lc, ap);
+    for (int it = 0;; ++it) {
+        const int row = blockIdx.x + it * gridDim.x;
+        if (row >= a.capacity)
+            break;
+        const int st = it % a.stages;
+        if (!mbar_wait(smem_addr(&s.full[st]), (uint32_t)(it / a.stages) & 1u, a.status))
+            break;
+        const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
+        const bool first = s.meta[st].first;
+        uint2 kvw[COFF * RATIO];
+        float2 e[COFF * RATIO][2], den[2], num[2];
+        pool_stage<RATIO, COFF>(stage, tc, lc, first, ap, kvw, e, den, num);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&s.empty[st]));
+        uint32_t o[2];
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            o[q] = f2_to_bf16x2(mul2(num[q], make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y))));
+        *reinterpret_cast<uint2 *>(out + (int64_t)row * a.head_dim + c0 + lc) = make_uint2(o[0], o[1]);
+    }
+}
+
+// ---------------------------------------------------------------- backward
+
+struct GradOut {
+    uint16_t *dkv;
+    uint16_t *dscore;
+    int64_t n_tokens;
+};
+
+template <int COFF>
+__device__ __forceinline__ void zero_range(const GradOut &o, int64_t C, int head_dim, int col, int64_t t0,
+                                           int64_t t1)
+{
+    t1 = t1 < o.n_tokens ? t1 : o.n_tokens;
+    for (int64_t t = t0 < 0 ? 0 : t0; t < t1; ++t) {
+#pragma unroll
+        for (int p = 0; p < COFF; ++p) {
+            *reinterpret_cast<uint2 *>(o.dkv + t * C + p * head_dim + col) = make_uint2(0u, 0u);
+            *reinterpret_cast<uint2 *>(o.dscore + t * C + p * head_dim + col) = make_uint2(0u, 0u);
+        }
+    }
+}
+
+// Gradient coverage as in csa_small.cu: a real row writes every slot it reads; the
+// last block of a segment zeroes its own first-half columns (coff 2) and the gap
+// up to the next real block (or n_tokens); block 0 zeroes the leading gap.  The
+// grad_ape partial of each thread block (its rows in ascending order, per thread)
+// is merged across the cluster in ascending rank order through distributed shared
+// memory; dape_finalize_kernel sums the cluster partials in a fixed order.
+template <int RATIO, int COFF>
+__global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n_tokens_arg,
+                                                         const uint16_t *__restrict__ grad_out,
+                                                         uint16_t *__restrict__ dkv, uint16_t *__restrict__ dscore,
+                                                         float *__restrict__ partial)
+{
+    constexpr int W = COFF * RATIO;
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const int ncw = blockDim.x / 32 - 1;
+    const int tc = ncw * 128;
+    const int c0 = blockIdx.y * tc;
+    const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t C = (int64_t)COFF * a.head_dim;
+    const int R = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;
+    const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
+    const int rend = R < a.capacity ? R : a.capacity;  // padding rows carry no gradient
+    GradOut o{dkv, dscore, n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg)};
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(smem_addr(&s.full[i]), 1);
+            mbar_init(smem_addr(&s.empty[i]), ncw);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    float2 acc[W][2];
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+        acc[k][0] = acc[k][1] = make_float2(0.0f, 0.0f);
+    const int lc = threadIdx.x * 4;
+    const int col = c0 + lc;
+
+    if (warp == ncw) {
+        if (lane == 0)
+            produce<RATIO, COFF, true>(a, s, tc, c0, blockIdx.x, gridDim.x, rend, grad_out);
+    } else {
+        if (blockIdx.x == 0) {  // leading gap: tokens before the first real block
+            int64_t lead = o.n_tokens;
+            if (R0 < R)
+                lead = map_row(R0, a.cu, a.cc, a.n_seg, RATIO).base;
+            zero_range<COFF>(o, C, a.head_dim, col, 0, lead);
+        }
+        ApeRegs<RATIO, COFF> ap;
+        load_ape<RATIO, COFF>(a, col, ap);
+        for (int it = 0;; ++it) {
+            const int row = blockIdx.x + it * gridDim.x;
+            if (row >= rend)
+                break;
+            const int st = it % a.stages;
+            if (!mbar_wait(smem_addr(&s.full[st]), (uint32_t)(it / a.stages) & 1u, a.status))
+                break;
+            const StageMeta m = s.meta[st];
+            if (!m.real) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&s.empty[st]));
+                continue;
+            }
+            const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
+            uint2 kvw[W];
+            float2 e[W][2], den[2], num[2];
+            pool_stage<RATIO, COFF>(stage, tc, lc, m.first, ap, kvw, e, den, num);
+            const uint2 gw = *reinterpret_cast<const uint2 *>(stage + window_bytes<RATIO, COFF>(tc) + lc * 2);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&s.empty[st]));
+            const float2 g[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
+            float2 inv[2], ngo[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                inv[q] = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
+                const float2 go = mul2(g[q], mul2(num[q], inv[q]));
+                ngo[q] = make_float2(-go.x, -go.y);
+            }
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (COFF == 2 && k < RATIO && m.first)
+                    continue;
+                const int p = k / RATIO, i = k % RATIO;
+                const int64_t tok = m.base + (int64_t)(p - (COFF - 1)) * RATIO + i;
+                const uint32_t kw[2] = {kvw[k].x, kvw[k].y};
+                uint32_t dk[2], dsw[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float2 pk = mul2(e[k][q], inv[q]);
+                    dk[q] = f2_to_bf16x2(mul2(g[q], pk));
+                    const float2 ds = mul2(pk, add2(mul2(g[q], bf16x2_to_f2(kw[q])), ngo[q]));
+                    dsw[q] = f2_to_bf16x2(ds);
+                    acc[k][q] = add2(acc[k][q], ds);
+                }
+                if (tok < o.n_tokens) {
+                    const int64_t gi = tok * C + (int64_t)p * a.head_dim + col;
+                    *reinterpret_cast<uint2 *>(dkv + gi) = make_uint2(dk[0], dk[1]);
+                    *reinterpret_cast<uint2 *>(dscore + gi) = make_uint2(dsw[0], dsw[1]);
+                }
+            }
+            if (m.row + 1 == __ldg(a.cc + m.seg + 1)) {  // last block of its segment
+                if (COFF == 2) {
+                    for (int i = 0; i < RATIO; ++i) {
+                        const int64_t tok = m.base + i;
+                        if (tok < o.n_tokens) {
+                            *reinterpret_cast<uint2 *>(dkv + tok * C + col) = make_uint2(0u, 0u);
+                            *reinterpret_cast<uint2 *>(dscore + tok * C + col) = make_uint2(0u, 0u);
+                        }
+                    }
+                }
+                int64_t next = o.n_tokens;
+                if (m.row + 1 < R)
+                    next = map_row(m.row + 1, a.cu, a.cc, a.n_seg, RATIO).base;
+                zero_range<COFF>(o, C, a.head_dim, col, m.base + RATIO, next);
+            }
+        }
+        // this thread's grad_ape sums -> shared memory [ape row][part][tile column]
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            const int p = k / RATIO, i = k % RATIO;
+            float *sp = s.red + (i * COFF + p) * tc + lc;
+            *reinterpret_cast<float4 *>(sp) = make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
+        }
+    }
+    __syncthreads();
+
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int rank = (int)cluster.block_rank();
+    const int nrank = (int)cluster.num_blocks();
+    const int n4 = RATIO * COFF * tc / 4;
+    const int share = (n4 + nrank - 1) / nrank;
+    const int i_lo = rank * share;
+    const int i_hi = i_lo + share < n4 ? i_lo + share : n4;
+    float *dst = partial + (int64_t)(blockIdx.x / nrank) * RATIO * C;
+    for (int i4 = i_lo + (int)threadIdx.x; i4 < i_hi; i4 += blockDim.x) {
+        const int rp = (i4 * 4) / tc, lcol = i4 * 4 - rp * tc;
+        const int arow = rp / COFF, p = rp - arow * COFF;
+        float4 acc4 = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(s.red, 0) + i4 * 4);
+        for (int q = 1; q < nrank; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(s.red, q) + i4 * 4);
+            acc4.x = __fadd_rn(acc4.x, v.x);
+            acc4.y = __fadd_rn(acc4.y, v.y);
+            acc4.z = __fadd_rn(acc4.z, v.z);
+            acc4.w = __fadd_rn(acc4.w, v.w);
+        }
+        *reinterpret_cast<float4 *>(dst + (int64_t)arow * C + (int64_t)p * a.head_dim + c0 + lcol) = acc4;
+    }
+    cluster.sync();
+}
+
+int tile_cols(int head_dim)
+{
+    for (int tc : {512, 384, 256, 128})
+        if (head_dim % tc == 0)
+            return tc;
+    return 0;
+}
+
+}  // namespace
+
+bool stream_supported(int ratio, int coff, int head_dim)
+{
+    return ratio == 4 && (coff == 1 || coff == 2) && head_dim % 128 == 0;
+}
+
+StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity, int num_sms)
+{
+    StreamPlan pl;
+    pl.tc = tile_cols(head_dim);
+    pl.tiles = head_dim / pl.tc;
+    pl.threads = (pl.tc / 128 + 1) * 32;
+    const int win = 2 * coff * ratio * pl.tc * 2;
+    pl.stage_bytes = ((bwd ? win + pl.tc * 2 : win) + 127) / 128 * 128;
+    const int budget = bwd ? 64 * 1024 : 96 * 1024;
+    pl.stages = budget / pl.stage_bytes;
+    pl.stages = pl.stages < 2 ? 2 : (pl.stages > 8 ? 8 : pl.stages);
+    pl.red_bytes = bwd ? (size_t)ratio * coff * pl.tc * sizeof(float) : 0;
+    pl.smem = smem_bytes(pl.stages, pl.stage_bytes, pl.red_bytes);
+    pl.cluster = bwd ? 4 : 1;
+    pl.num_sms = num_sms;
+    (void)capacity;
+    return pl;
+}
+
+template <int RATIO, int COFF>
+static cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out)
+{
+    const void *fn = bwd ? reinterpret_cast<const void *>(bwd_stream_kernel<RATIO, COFF>)
+                         : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF>);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, pl.threads, pl.smem);
+    if (e != cudaSuccess)
+        return e;
+    int blocks = (per_sm > 0 ? per_sm : 1) * pl.num_sms / pl.tiles;
+    if (blocks < 1)
+        blocks = 1;
+    if (blocks > rows)
+        blocks = rows > 0 ? rows : 1;
+    blocks = (blocks + pl.cluster - 1) / pl.cluster * pl.cluster;
+    *out = blocks;
+    return cudaSuccess;
+}
+
+template <int RATIO, int COFF>
+static cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl, unsigned *status,
+                                       cudaStream_t st)
+{
+    StreamArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
+                 p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes,
+                 status};
+    int blocks = 0;
+    cudaError_t e = blocks_for<RATIO, COFF>(pl, false, p.capacity, &blocks);
+    if (e != cudaSuccess)
+        return e;
+    fwd_stream_kernel<RATIO, COFF><<<dim3(blocks, pl.tiles), pl.threads, pl.smem, st>>>(
+        a, static_cast<uint16_t *>(p.out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st)
+{
+    if (p.ratio == 4 && p.coff == 2)
+        return launch_fwd_stream_t<4, 2>(p, pl, status, st);
+    if (p.ratio == 4 && p.coff == 1)
+        return launch_fwd_stream_t<4, 1>(p, pl, status, st);
+    return cudaErrorInvalidValue;
+}
+
+// Upper bound of grad_ape partials (cluster count) for the workspace size.
+int stream_bwd_partials(const StreamPlan &pl, int capacity)
+{
+    const int rows = capacity > 0 ? capacity : 1;
+    int blocks = 8 * pl.num_sms / pl.tiles;  // never more than 8 resident per SM
+    if (blocks > rows)
+        blocks = rows;
+    blocks = (blocks + pl.cluster - 1) / pl.cluster * pl.cluster;
+    return blocks / pl.cluster;
+}
+
+template <int RATIO, int COFF>
+static cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
+                                       cudaStream_t st)
+{
+    StreamArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
+                 p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes,
+                 status};
+    int blocks = 0;
+    cudaError_t e = blocks_for<RATIO, COFF>(pl, true, p.capacity, &blocks);
+    if (e != cudaSuccess)
+        return e;
+    const int max_blocks = stream_bwd_partials(pl, p.capacity) * pl.cluster;
+    if (blocks > max_blocks)
+        blocks = max_blocks;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, pl.tiles, 1);
+    cfg.blockDim = dim3(pl.threads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_stream_kernel<RATIO, COFF>, a, p.n_tokens,
+                           static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
+                           static_cast<uint16_t *>(p.dscore), partial);
+    if (e != cudaSuccess)
+        return e;
+    return launch_dape_finalize(partial, blocks / pl.cluster, (int64_t)RATIO * COFF * p.head_dim, p.dape, st);
+}
+
+cudaError_t launch_bwd_stream(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
+                              cudaStream_t st)
+{
+    if (p.ratio == 4 && p.coff == 2)
+        return launch_bwd_stream_t<4, 2>(p, pl, partial, status, st);
+    if (p.ratio == 4 && p.coff == 1)
+        return launch_bwd_stream_t<4, 1>(p, pl, partial, status, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace csa

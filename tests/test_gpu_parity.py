@@ -189,3 +189,20 @@ def test_misaligned_view_is_rejected_and_nothing_written(csa):
     assert ei.value.status == 3
     torch.cuda.synchronize()
     assert (out == -1).all()
+
+
+def test_both_kernel_families_agree_bitwise(csa):
+    """head_dim 384 (a multiple of 128: the bulk-copy pipeline) and 392 (not: the
+    register kernels) on the same rows give the oracle's bits in both."""
+    for D in (384, 392):
+        c = w.make_case("fam", 4, 2, D, [57, 4, 130], extra_rows=2, seed=12)
+        d = Dev(c)
+        assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))
+        dkv, dsc, _ = run_bwd(d, csa)
+        want = oracle.case_bwd_f32(c)
+        assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+
+
+def test_zz_no_bounded_wait_expired(csa):
+    """No kernel of this module recorded a timeout in the device status word."""
+    assert csa.csa_device_status(clear=True) == 0
