@@ -227,10 +227,16 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
     csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
     const bool streamed = csa::stream_supported(ratio, coff, head_dim);
-    const csa::StreamPlan sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, ds->num_sms);
-    const csa::SmallBwdPlan pl = csa::plan_bwd_small(ratio, coff, head_dim, capacity, ds->num_sms);
-    const int64_t floats = streamed ? (int64_t)csa::stream_bwd_partials(sp, capacity) * ratio * coff * head_dim
-                                    : pl.partial_floats;
+    csa::StreamPlan sp{};
+    csa::SmallBwdPlan pl{};
+    int64_t floats = 0;
+    if (streamed) {
+        sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, ds->num_sms);
+        floats = (int64_t)csa::stream_bwd_partials(sp, capacity) * ratio * coff * head_dim;
+    } else {
+        pl = csa::plan_bwd_small(ratio, coff, head_dim, capacity, ds->num_sms);
+        floats = pl.partial_floats;
+    }
     void *partial = nullptr;
     e = cudaMallocFromPoolAsync(&partial, (size_t)floats * sizeof(float), ds->pool, st);
     if (e != cudaSuccess)

@@ -69,8 +69,8 @@ __device__ __forceinline__ float2 exp2lanes(float2 x)
     p = fma2(p, r, splat(1.0f));
     // bits(t) = bits(kRound) + n; bits(kRound) << 23 vanishes mod 2^32, so
     // (bits(t) << 23) + bias is the bit pattern of 2^n (and +0 for n = -127).
-    const float2 scale = make_float2(__uint_as_float(__float_as_uint(t.x) * 8388608u + 0x3f800000u),
-                                     __uint_as_float(__float_as_uint(t.y) * 8388608u + 0x3f800000u));
+    const float2 scale = make_float2(__uint_as_float((__float_as_uint(t.x) << 23) + 0x3f800000u),
+                                     __uint_as_float((__float_as_uint(t.y) << 23) + 0x3f800000u));
     return mul2(p, scale);
 }
 
@@ -78,7 +78,8 @@ __device__ __forceinline__ float2 exp2lanes(float2 x)
 // A 32-bit word holding two bf16 (low half = lower column) <-> an fp32 pair.
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
 {
-    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    // byte permutes: (w.b1 w.b0 0 0) and (w.b3 w.b2 0 0)
+    return make_float2(__uint_as_float(__byte_perm(w, 0u, 0x1044u)), __uint_as_float(__byte_perm(w, 0u, 0x3244u)));
 }
 
 // Round an fp32 pair to bf16, nearest-even (cvt.rn), lower column in the low half.

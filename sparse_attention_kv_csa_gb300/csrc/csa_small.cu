@@ -294,10 +294,10 @@ __global__ void __launch_bounds__(kFwdThreads, CSA_FWD_MINB) fwd_small_kernel(Sm
 // ------------------------------------------------------------- backward
 
 #ifndef CSA_BWD_NW
-#define CSA_BWD_NW 2
+#define CSA_BWD_NW 1
 #endif
 #ifndef CSA_BWD_MINB
-#define CSA_BWD_MINB 3
+#define CSA_BWD_MINB 4
 #endif
 #ifndef CSA_BWD_CLUSTER
 #define CSA_BWD_CLUSTER 4

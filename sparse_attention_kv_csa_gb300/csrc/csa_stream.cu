@@ -29,6 +29,17 @@
 
 namespace cg = cooperative_groups;
 
+// Ring sizes (bytes of stages per block) and the backward's cluster size.
+#ifndef CSA_STREAM_FWD_BUDGET
+#define CSA_STREAM_FWD_BUDGET (64 * 1024)
+#endif
+#ifndef CSA_STREAM_BWD_BUDGET
+#define CSA_STREAM_BWD_BUDGET (64 * 1024)
+#endif
+#ifndef CSA_STREAM_BWD_CLUSTER
+#define CSA_STREAM_BWD_CLUSTER 4
+#endif
+
 namespace csa {
 
 namespace {
@@ -108,13 +119,9 @@ __device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int 
 {
     const int64_t C = (int64_t)COFF * a.head_dim;
     const uint32_t run = (uint32_t)tc * 2;
-    int issued = 0;
-    for (int it = 0;; ++it) {
-        const int row = row0 + it * rstride;
-        if (row >= rend)
-            break;
-        const int st = it % a.stages;
-        const uint32_t ph = (uint32_t)(it / a.stages) & 1u;
+    int issued = 0, st = 0;
+    uint32_t ph = 0;
+    for (int row = row0; row < rend; row += rstride) {
         if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
             break;
         const RowMap rm = map_row(row, a.cu, a.cc, a.n_seg, RATIO);
@@ -144,7 +151,11 @@ __device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int 
             if (BWD)
                 bulk_g2s(dst + window_bytes<RATIO, COFF>(tc), grad_out + (int64_t)row * a.head_dim + c0, run, fb);
         }
-        issued = it + 1;
+        ++issued;
+        if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
     }
     // Copies of the last (up to) `stages` rows may still be in flight if the
     // consumers stopped early: wait for them before the block may exit.
@@ -251,12 +262,10 @@ __global__ void __launch_bounds__(160) fwd_stream_kernel(StreamArgs a, uint16_t 
     const int lc = threadIdx.x * 4;  // local column of this thread in the tile
     ApeRegs<RATIO, COFF> ap;
     load_ape<RATIO, COFF>(a, c0 + lc, ap);
-    for (int it = 0;; ++it) {
-        const int row = blockIdx.x + it * gridDim.x;
-        if (row >= a.capacity)
-            break;
-        const int st = it % a.stages;
-        if (!mbar_wait(smem_addr(&s.full[st]), (uint32_t)(it / a.stages) & 1u, a.status))
+    int st = 0;
+    uint32_t ph = 0;
+    for (int row = blockIdx.x; row < a.capacity; row += gridDim.x) {
+        if (!mbar_wait(smem_addr(&s.full[st]), ph, a.status))
             break;
         const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
         const bool first = s.meta[st].first;
@@ -271,6 +280,10 @@ __global__ void __launch_bounds__(160) fwd_stream_kernel(StreamArgs a, uint16_t 
         for (int q = 0; q < 2; ++q)
             o[q] = f2_to_bf16x2(mul2(num[q], make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y))));
         *reinterpret_cast<uint2 *>(out + (int64_t)row * a.head_dim + c0 + lc) = make_uint2(o[0], o[1]);
+        if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
     }
 }
 
@@ -348,28 +361,31 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
         }
         ApeRegs<RATIO, COFF> ap;
         load_ape<RATIO, COFF>(a, col, ap);
-        for (int it = 0;; ++it) {
-            const int row = blockIdx.x + it * gridDim.x;
-            if (row >= rend)
-                break;
-            const int st = it % a.stages;
-            if (!mbar_wait(smem_addr(&s.full[st]), (uint32_t)(it / a.stages) & 1u, a.status))
+        int st = 0;
+        uint32_t ph = 0;
+        for (int row = blockIdx.x; row < rend; row += gridDim.x) {
+            if (!mbar_wait(smem_addr(&s.full[st]), ph, a.status))
                 break;
             const StageMeta m = s.meta[st];
+            const int st_used = st;
+            if (++st == a.stages) {
+                st = 0;
+                ph ^= 1u;
+            }
             if (!m.real) {
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(smem_addr(&s.empty[st]));
+                    mbar_arrive(smem_addr(&s.empty[st_used]));
                 continue;
             }
-            const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
+            const unsigned char *stage = s.stages + (size_t)st_used * a.stage_bytes;
             uint2 kvw[W];
             float2 e[W][2], den[2], num[2];
             pool_stage<RATIO, COFF>(stage, tc, lc, m.first, ap, kvw, e, den, num);
             const uint2 gw = *reinterpret_cast<const uint2 *>(stage + window_bytes<RATIO, COFF>(tc) + lc * 2);
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(smem_addr(&s.empty[st]));
+                mbar_arrive(smem_addr(&s.empty[st_used]));
             const float2 g[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
             float2 inv[2], ngo[2];
 #pragma unroll
@@ -474,12 +490,12 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     pl.threads = (pl.tc / 128 + 1) * 32;
     const int win = 2 * coff * ratio * pl.tc * 2;
     pl.stage_bytes = ((bwd ? win + pl.tc * 2 : win) + 127) / 128 * 128;
-    const int budget = bwd ? 64 * 1024 : 96 * 1024;
+    const int budget = bwd ? CSA_STREAM_BWD_BUDGET : CSA_STREAM_FWD_BUDGET;
     pl.stages = budget / pl.stage_bytes;
     pl.stages = pl.stages < 2 ? 2 : (pl.stages > 8 ? 8 : pl.stages);
     pl.red_bytes = bwd ? (size_t)ratio * coff * pl.tc * sizeof(float) : 0;
     pl.smem = smem_bytes(pl.stages, pl.stage_bytes, pl.red_bytes);
-    pl.cluster = bwd ? 4 : 1;
+    pl.cluster = bwd ? CSA_STREAM_BWD_CLUSTER : 1;
     pl.num_sms = num_sms;
     (void)capacity;
     return pl;
@@ -493,11 +509,34 @@ static cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess)
         return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, pl.threads, pl.smem);
-    if (e != cudaSuccess)
-        return e;
-    int blocks = (per_sm > 0 ? per_sm : 1) * pl.num_sms / pl.tiles;
+    int resident = 0;
+    if (pl.cluster > 1) {
+        // clusters are placed within GPCs: ask how many fit, not blocks per SM
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(pl.cluster, 1, 1);
+        cfg.blockDim = dim3(pl.threads, 1, 1);
+        cfg.dynamicSmemBytes = pl.smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = pl.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        resident = clusters * pl.cluster;
+    } else {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, pl.threads, pl.smem);
+        if (e != cudaSuccess)
+            return e;
+        resident = per_sm * pl.num_sms;
+    }
+    int blocks = (resident > 0 ? resident : 1) / pl.tiles;
+    blocks = blocks / pl.cluster * pl.cluster;
     if (blocks < 1)
         blocks = 1;
     if (blocks > rows)
