@@ -118,6 +118,33 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
                      float *dape, void *stream);
 
 /*
+ * Backward pass that allocates nothing.  The page has no counterpart of this call:
+ * it is an addition of this library for callers that cannot allocate device
+ * memory inside the call -- a framework that has reserved all of HBM for its own
+ * arena up front, a real-time loop in which growing or trimming a memory pool
+ * could block, a plug-in that may not use the CUDA allocator.
+ *
+ * Same arguments, results and errors as csa_compress_bwd (bitwise the same
+ * outputs), except that the grad_ape partial sums go to a fixed 2 MiB array in
+ * the library's device code instead of the library's memory pool.  That array
+ * occupies 2 MiB on every GPU that loads the library, until the process exits.
+ * A shape that needs more partial storage than the array holds is rejected with
+ * CSA_ERR_TOO_LARGE before anything is launched (no ratio-4 shape does on a
+ * 152-SM GB300).  No cudaMalloc, cudaFree or other allocating call is made.
+ *
+ * Every call on a device shares the array and leaves its contents behind; each
+ * call writes all it reads, so nothing needs clearing, but calls that overlap on
+ * the GPU (different streams or host threads) race: order them.  The first call
+ * on a device (with that device current) looks up the array's device address;
+ * make that first call before any stream capture.
+ */
+CSA_API int csa_compress_bwd_noalloc(const void *kv, const void *score, const float *ape,
+                             const int32_t *cu_seqlens, const int32_t *cu_seqlens_comp, int32_t n_seg,
+                             int32_t ratio, int32_t coff, int32_t head_dim, int32_t capacity,
+                             int64_t n_tokens, const void *grad_out, void *dkv, void *dscore,
+                             float *dape, void *stream);
+
+/*
  * Host-only support check ("CSA Fused Compressor", section Support surface):
  * CSA_OK if (ratio, coff, head_dim) has a kernel and the sizes fit the int32
  * flat-offset bounds (n_tokens * coff * head_dim < 2^31, capacity * head_dim <

@@ -29,7 +29,7 @@ import os
 from . import _build
 
 __all__ = [
-    "csa_compress_fwd", "csa_compress_bwd", "csa_check_support", "csa_status_string",
+    "csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support", "csa_status_string",
     "csa_last_error_message", "csa_version", "csa_device_status", "CSAError", "compress_forward", "compress_backward",
     "library_path", "STATUS",
 ]
@@ -53,13 +53,15 @@ def _load():
     common = [P, P, P, P, P, i32, i32, i32, i32, i32]
     lib.csa_compress_fwd.argtypes = common + [P, P]
     lib.csa_compress_bwd.argtypes = common + [i64, P, P, P, P, P]
+    lib.csa_compress_bwd_noalloc.argtypes = common + [i64, P, P, P, P, P]
     lib.csa_check_support.argtypes = [i32, i32, i32, i64, i32]
     lib.csa_device_status.argtypes = [ctypes.c_int]
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_last_error_message.argtypes = []
     lib.csa_last_error_message.restype = ctypes.c_char_p
-    for f in ("csa_compress_fwd", "csa_compress_bwd", "csa_check_support", "csa_version", "csa_device_status"):
+    for f in ("csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support",
+              "csa_version", "csa_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -127,6 +129,16 @@ def csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, 
                                  _addr(cu_seqlens_comp), n_seg, ratio, coff, head_dim, capacity,
                                  n_tokens, _addr(grad_out), _addr(dkv), _addr(dscore), _addr(dape),
                                  _stream(stream)))
+
+
+def csa_compress_bwd_noalloc(kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
+                             capacity, n_tokens, grad_out, dkv, dscore, dape, stream=None) -> None:
+    """csa_compress_bwd for callers that cannot allocate: its scratch is a fixed
+    2 MiB array of the library (shared by all calls on a device; see csa.h)."""
+    _check(_lib.csa_compress_bwd_noalloc(_addr(kv), _addr(score), _addr(ape), _addr(cu_seqlens),
+                                         _addr(cu_seqlens_comp), n_seg, ratio, coff, head_dim, capacity,
+                                         n_tokens, _addr(grad_out), _addr(dkv), _addr(dscore), _addr(dape),
+                                         _stream(stream)))
 
 
 def compress_forward(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim, capacity,

@@ -141,6 +141,19 @@ int check_ptr(const void *p, const char *name, uintptr_t align)
 
 }  // namespace
 
+namespace csa {
+
+int fail_status(int status, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+}  // namespace csa
+
 extern "C" {
 
 int csa_version(void) { return 100; }

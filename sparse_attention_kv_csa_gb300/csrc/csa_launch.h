@@ -76,6 +76,11 @@ int stream_bwd_partials(const StreamPlan &pl, int capacity);
 cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st);
 cudaError_t launch_bwd_stream(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
                               cudaStream_t st);
+// The exact grid width launch_bwd_stream uses (partials = blocks / pl.cluster).
+cudaError_t stream_bwd_blocks(int ratio, int coff, const StreamPlan &pl, int capacity, int *blocks);
+
+// Records a status and the thread-local message returned by csa_last_error_message().
+int fail_status(int status, const char *fmt, ...);
 SmallBwdPlan plan_bwd_small(int ratio, int coff, int head_dim, int capacity, int num_sms);
 cudaError_t launch_bwd_small(const BwdParams &p, const SmallBwdPlan &pl, float *partial, cudaStream_t st);
 

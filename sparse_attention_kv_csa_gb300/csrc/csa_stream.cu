@@ -616,6 +616,27 @@ static cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl,
     return launch_dape_finalize(partial, blocks / pl.cluster, (int64_t)RATIO * COFF * p.head_dim, p.dape, st);
 }
 
+template <int RATIO, int COFF>
+static cudaError_t stream_bwd_blocks_t(const StreamPlan &pl, int capacity, int *out)
+{
+    int blocks = 0;
+    cudaError_t e = blocks_for<RATIO, COFF>(pl, true, capacity, &blocks);
+    if (e != cudaSuccess)
+        return e;
+    const int max_blocks = stream_bwd_partials(pl, capacity) * pl.cluster;
+    *out = blocks > max_blocks ? max_blocks : blocks;
+    return cudaSuccess;
+}
+
+cudaError_t stream_bwd_blocks(int ratio, int coff, const StreamPlan &pl, int capacity, int *blocks)
+{
+    if (ratio == 4 && coff == 2)
+        return stream_bwd_blocks_t<4, 2>(pl, capacity, blocks);
+    if (ratio == 4 && coff == 1)
+        return stream_bwd_blocks_t<4, 1>(pl, capacity, blocks);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_bwd_stream(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
                               cudaStream_t st)
 {

@@ -1,0 +1,65 @@
+"""csa_compress_bwd_noalloc: the backward for callers that cannot allocate device
+memory inside the call (its scratch is a fixed array in the library's device
+code).  Checked through the C ABI against csa_compress_bwd on the same inputs,
+for two calls in a row (the second on different data, so that anything the
+first call left in the shared scratch would show), in both kernel families.
+
+This file sorts last so that a run stopping at the first failure has already
+run every other test; it also passes alone in a fresh process.
+"""
+import numpy as np
+import pytest
+
+import csa_workloads as w
+from gpu_util import Dev, F, run_bwd
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa():
+    import sparse_attention_kv_csa_gb300 as m
+    return m
+
+
+def run_noalloc(d, csa, canary):
+    import torch
+    c = d.c
+    C = c.coff * c.head_dim
+    fill = np.int16(np.uint16(canary).view(np.int16))
+    dkv = torch.full((c.n_tokens, C), fill, dtype=torch.int16, device="cuda")
+    dsc = torch.full((c.n_tokens, C), fill, dtype=torch.int16, device="cuda")
+    dape = torch.full((c.ratio, C), float("nan"), dtype=torch.float32, device="cuda")
+    csa.csa_compress_bwd_noalloc(d.kv, d.score, d.ape, d.cu, d.cc, c.n_seg, c.ratio, c.coff, c.head_dim,
+                                 c.capacity, c.n_tokens, d.g, dkv, dsc, dape)
+    torch.cuda.synchronize()
+    return dkv.cpu().numpy().view(np.uint16), dsc.cpu().numpy().view(np.uint16), dape.cpu().numpy()
+
+
+@pytest.mark.parametrize("head_dim", [512, 64])  # bulk-copy pipeline / register kernels
+def test_noalloc_matches_backward_two_calls_in_a_row(csa, head_dim):
+    cases = [w.make_case("na%d" % s, 4, 2, head_dim, [4096, 37, 2, 1100], extra_rows=16, seed=s)
+             for s in (31, 32)]
+    for c, canary in zip(cases, (0xFFFF, 0x7FC1)):
+        d = Dev(c)
+        want_dkv, want_dsc, want_dape = run_bwd(d, csa)
+        got_dkv, got_dsc, got_dape = run_noalloc(d, csa, canary)
+        assert np.array_equal(got_dkv, want_dkv)
+        assert np.array_equal(got_dsc, want_dsc)
+        assert np.isfinite(got_dape).all()
+        assert np.abs(got_dape - want_dape).max() <= 1e-5 * np.abs(want_dape).max()
+    assert csa.csa_device_status() == 0
+
+
+def test_noalloc_rejects_bad_arguments_before_launch(csa):
+    import torch
+    c = w.make_case("na_bad", 4, 2, 512, [64], seed=3)
+    d = Dev(c)
+    dkv = torch.zeros((c.n_tokens, 1024), dtype=torch.int16, device="cuda")
+    dape = torch.zeros((4, 1024), dtype=torch.float32, device="cuda")
+    with pytest.raises(csa.CSAError) as ei:
+        csa.csa_compress_bwd_noalloc(d.kv, d.score, d.ape, d.cu, d.cc, c.n_seg, 4, 2, 512, c.capacity,
+                                     c.n_tokens, d.g, dkv, dkv, dape.view(-1)[1:].data_ptr())
+    assert ei.value.status == 3  # misaligned dape
+    torch.cuda.synchronize()
+    assert not dkv.any()
