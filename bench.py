@@ -396,10 +396,10 @@ def main():
                 "gbs": gbs(fwd_b, ms_fwd), "frac_of_peak": gbs(fwd_b, ms_fwd) / peak},
         "bwd": {"ms": ms_bwd, "tokens_per_s": world * tokens / (ms_bwd * 1e-3), "bytes": bwd_b,
                 "gbs": gbs(bwd_b, ms_bwd), "frac_of_peak": gbs(bwd_b, ms_bwd) / peak},
-        "roofline": {"bound": "hbm", "kernel": "csa_compress_bwd (bwd_small_kernel + dape_finalize_kernel)",
+        "roofline": {"bound": "hbm", "kernel": "csa_compress_bwd call: bwd_stream_kernel + dape_finalize_kernel",
                      "achieved": gbs(bwd_b, ms_bwd), "peak": peak, "peak_source": peak_kind + " hbm_gbs",
                      "unit": "GB/s", "frac": gbs(bwd_b, ms_bwd) / peak,
-                     "traffic": recorded_traffic("bwd_small_kernel:" + c.name)},
+                     "traffic": recorded_traffic("csa_compress_bwd:" + c.name)},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }

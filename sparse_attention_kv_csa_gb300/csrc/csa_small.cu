@@ -432,6 +432,8 @@ __global__ void __launch_bounds__(kBwdThreads, CSA_BWD_MINB)
     constexpr int W = COFF * RATIO;
     constexpr int NW = kBwdNW;
     extern __shared__ float red[];
+    // Let the grad_ape finalisation grid launch now; it waits for this grid's end.
+    asm volatile("griddepcontrol.launch_dependents;");
     const int lanes = blockDim.y;
     const int x = threadIdx.x, y = threadIdx.y;
     const int j = (blockIdx.y * blockDim.x + x) * (2 * NW);
@@ -544,20 +546,24 @@ __global__ void __launch_bounds__(kBwdThreads, CSA_BWD_MINB)
 
 }  // namespace
 
-// grad_ape = the partials summed in a fixed order.  Eight threads per 4-float
-// column: thread t adds partials [t*P/8, (t+1)*P/8) in ascending order, then the
-// eight subtotals are combined by a fixed butterfly ((s0+s1)+(s2+s3))+((s4+s5)+(s6+s7)).
+// grad_ape = the partials summed in a fixed order.  One warp per 4-float column:
+// lane l adds partials [l*P/32, (l+1)*P/32) in ascending order, then the 32
+// subtotals are combined by a fixed butterfly (xor 1, 2, 4, 8, 16).
+// Launched as a programmatic dependent of the backward kernel: griddepcontrol.wait
+// holds it until that grid has finished and its partials are visible (a plain
+// launch returns from the wait at once).
 __global__ void __launch_bounds__(256) dape_finalize_kernel(const float *__restrict__ partial,
                                                             int n_partials, int64_t n,
                                                             float *__restrict__ dape)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t i = gt >> 3;
-    const int t = (int)(gt & 7);
+    const int64_t i = gt >> 5;
+    const int t = (int)(gt & 31);
     const int64_t stride = n / 4;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (i < stride) {
-        const int lo = (int)((int64_t)t * n_partials / 8), hi = (int)((int64_t)(t + 1) * n_partials / 8);
+        const int lo = (int)((int64_t)t * n_partials / 32), hi = (int)((int64_t)(t + 1) * n_partials / 32);
         const float4 *p = reinterpret_cast<const float4 *>(partial) + i;
         int b = lo;
         for (; b + 4 <= hi; b += 4) {
@@ -582,7 +588,7 @@ __global__ void __launch_bounds__(256) dape_finalize_kernel(const float *__restr
         }
     }
 #pragma unroll
-    for (int m = 1; m < 8; m <<= 1) {
+    for (int m = 1; m < 32; m <<= 1) {
         acc.x = __fadd_rn(acc.x, __shfl_xor_sync(0xffffffffu, acc.x, m));
         acc.y = __fadd_rn(acc.y, __shfl_xor_sync(0xffffffffu, acc.y, m));
         acc.z = __fadd_rn(acc.z, __shfl_xor_sync(0xffffffffu, acc.z, m));
@@ -596,9 +602,17 @@ __global__ void __launch_bounds__(256) dape_finalize_kernel(const float *__restr
 
 cudaError_t launch_dape_finalize(const float *partial, int n_partials, int64_t n, float *dape, cudaStream_t st)
 {
-    const int64_t threads = n / 4 * 8;
-    dape_finalize_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, n_partials, n, dape);
-    return cudaGetLastError();
+    const int64_t threads = n / 4 * 32;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((threads + 255) / 256), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dape_finalize_kernel, partial, n_partials, n, dape);
 }
 
 template <int RATIO, int COFF>
@@ -607,11 +621,19 @@ static cudaError_t launch_fwd_small_t(const FwdParams &p, int num_sms, cudaStrea
     SmallArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
                 p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity};
     const int64_t units = (int64_t)p.capacity * (p.head_dim / (2 * kFwdNW));
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_small_kernel<RATIO, COFF>,
-                                                                  kFwdThreads, 0);
+    static int cached_per_sm[64] = {0};  // per device; occupancy is a slow host query
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    int per_sm = (dev >= 0 && dev < 64) ? cached_per_sm[dev] : 0;
+    if (per_sm == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_small_kernel<RATIO, COFF>, kFwdThreads, 0);
+        if (e != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < 64)
+            cached_per_sm[dev] = per_sm;
+    }
     int64_t grid = (units + kFwdThreads - 1) / kFwdThreads;
     const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * num_sms;
     if (grid > resident)
@@ -684,10 +706,7 @@ static cudaError_t launch_bwd_small_t(const BwdParams &p, const SmallBwdPlan &pl
                                        static_cast<uint16_t *>(p.dscore), partial);
     if (e != cudaSuccess)
         return e;
-    const int64_t n = (int64_t)RATIO * COFF * p.head_dim;
-    const int64_t threads = n / 4 * 8;
-    dape_finalize_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(partial, pl.partials, n, p.dape);
-    return cudaGetLastError();
+    return launch_dape_finalize(partial, pl.partials, (int64_t)RATIO * COFF * p.head_dim, p.dape, st);
 }
 
 cudaError_t launch_bwd_small(const BwdParams &p, const SmallBwdPlan &pl, float *partial, cudaStream_t st)

@@ -24,6 +24,8 @@
 // normally (no trap, no hang).
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "csa_device.cuh"
 #include "csa_launch.h"
 
@@ -37,7 +39,11 @@ namespace cg = cooperative_groups;
 #define CSA_STREAM_BWD_BUDGET (64 * 1024)
 #endif
 #ifndef CSA_STREAM_BWD_CLUSTER
-#define CSA_STREAM_BWD_CLUSTER 4
+#define CSA_STREAM_BWD_CLUSTER 2
+#endif
+// Blocks per SM the forward's registers are capped for (1: no cap).
+#ifndef CSA_STREAM_FWD_MINB
+#define CSA_STREAM_FWD_MINB 1
 #endif
 
 namespace csa {
@@ -238,7 +244,7 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int tc, i
 // ----------------------------------------------------------------- forward
 
 template <int RATIO, int COFF>
-__global__ void __launch_bounds__(160) fwd_stream_kernel(StreamArgs a, uint16_t *__restrict__ out)
+__global__ void __launch_bounds__(160, CSA_STREAM_FWD_MINB) fwd_stream_kernel(StreamArgs a, uint16_t *__restrict__ out)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int ncw = blockDim.x / 32 - 1;  // consumer warps; the last warp produces
@@ -333,6 +339,8 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
     const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
     const int rend = R < a.capacity ? R : a.capacity;  // padding rows carry no gradient
     GradOut o{dkv, dscore, n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg)};
+    // Let the grad_ape finalisation grid launch now; it waits for this grid's end.
+    asm volatile("griddepcontrol.launch_dependents;");
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(smem_addr(&s.full[i]), 1);
@@ -501,40 +509,88 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     return pl;
 }
 
-template <int RATIO, int COFF>
-static cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out)
+// Resident blocks of a kernel configuration, computed once per (device, kernel,
+// block size, shared memory, cluster) and cached: the occupancy queries and the
+// shared-memory attribute are host calls too slow to repeat on every launch.
+struct ResidentKey {
+    int dev;
+    const void *fn;
+    int threads;
+    size_t smem;
+    int cluster;
+};
+
+static cudaError_t cached_resident(const ResidentKey &k, int *resident, cudaError_t (*query)(const ResidentKey &, int *))
 {
-    const void *fn = bwd ? reinterpret_cast<const void *>(bwd_stream_kernel<RATIO, COFF>)
-                         : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF>);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    static std::mutex mu;
+    static ResidentKey keys[64];
+    static int vals[64];
+    static int n = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (int i = 0; i < n; ++i)
+            if (keys[i].dev == k.dev && keys[i].fn == k.fn && keys[i].threads == k.threads &&
+                keys[i].smem == k.smem && keys[i].cluster == k.cluster) {
+                *resident = vals[i];
+                return cudaSuccess;
+            }
+    }
+    cudaError_t e = query(k, resident);
     if (e != cudaSuccess)
         return e;
-    int resident = 0;
-    if (pl.cluster > 1) {
+    std::lock_guard<std::mutex> g(mu);
+    if (n < 64) {
+        keys[n] = k;
+        vals[n] = *resident;
+        ++n;
+    }
+    return cudaSuccess;
+}
+
+static cudaError_t query_resident(const ResidentKey &k, int *resident)
+{
+    cudaError_t e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem);
+    if (e != cudaSuccess)
+        return e;
+    if (k.cluster > 1) {
         // clusters are placed within GPCs: ask how many fit, not blocks per SM
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(pl.cluster, 1, 1);
-        cfg.blockDim = dim3(pl.threads, 1, 1);
-        cfg.dynamicSmemBytes = pl.smem;
+        cfg.gridDim = dim3(k.cluster, 1, 1);
+        cfg.blockDim = dim3(k.threads, 1, 1);
+        cfg.dynamicSmemBytes = k.smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = pl.cluster;
+        attr[0].val.clusterDim.x = k.cluster;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
-        if (e != cudaSuccess)
-            return e;
-        resident = clusters * pl.cluster;
-    } else {
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, pl.threads, pl.smem);
-        if (e != cudaSuccess)
-            return e;
-        resident = per_sm * pl.num_sms;
+        e = cudaOccupancyMaxActiveClusters(&clusters, k.fn, &cfg);
+        *resident = clusters * k.cluster;
+        return e;
     }
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, k.threads, k.smem);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, k.dev);
+    *resident = per_sm * sms;
+    return e;
+}
+
+template <int RATIO, int COFF>
+static cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out)
+{
+    const void *fn = bwd ? reinterpret_cast<const void *>(bwd_stream_kernel<RATIO, COFF>)
+                         : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF>);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    int resident = 0;
+    e = cached_resident(ResidentKey{dev, fn, pl.threads, pl.smem, pl.cluster}, &resident, query_resident);
+    if (e != cudaSuccess)
+        return e;
     int blocks = (resident > 0 ? resident : 1) / pl.tiles;
     blocks = blocks / pl.cluster * pl.cluster;
     if (blocks < 1)
