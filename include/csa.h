@@ -46,7 +46,12 @@
  * calling thread's last non-OK return.
  *
  * Supported set (csa_check_support): coff in {1, 2}; ratio == 4 with head_dim a
- * multiple of 8 in [8, 8192].
+ * multiple of 8 in [8, 8192]; ratio == 128 with head_dim a multiple of 64 in
+ * [64, 8192].  Numerics per ratio family (section Numerics): ratio 4 computes
+ * every window in ascending position order (bitwise equal to a plain sequential
+ * fp32 evaluation with the library's exp); ratio 128 sums the window in fixed
+ * chunks (deterministic, equal to the sequential evaluation within final-bf16
+ * rounding tolerance).
  */
 #ifndef CSA_H_
 #define CSA_H_
@@ -125,12 +130,13 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * could block, a plug-in that may not use the CUDA allocator.
  *
  * Same arguments, results and errors as csa_compress_bwd (bitwise the same
- * outputs), except that the grad_ape partial sums go to a fixed 2 MiB array in
+ * outputs), except that the grad_ape partial sums go to a fixed 4 MiB array in
  * the library's device code instead of the library's memory pool.  That array
- * occupies 2 MiB on every GPU that loads the library, until the process exits.
+ * occupies 4 MiB on every GPU that loads the library, until the process exits.
  * A shape that needs more partial storage than the array holds is rejected with
- * CSA_ERR_TOO_LARGE before anything is launched (no ratio-4 shape does on a
- * 152-SM GB300).  No cudaMalloc, cudaFree or other allocating call is made.
+ * CSA_ERR_TOO_LARGE before anything is launched (on a 152-SM GB300 every ratio-4
+ * shape fits, and ratio-128 shapes up to coff * head_dim = 1024).  No cudaMalloc,
+ * cudaFree or other allocating call is made.
  *
  * Every call on a device shares the array and leaves its contents behind; each
  * call writes all it reads, so nothing needs clearing, but calls that overlap on

@@ -100,8 +100,12 @@ int check_common(int32_t n_seg, int32_t ratio, int32_t coff, int32_t head_dim, i
         if (head_dim % 8 != 0 || head_dim > 8192)
             return fail(CSA_ERR_UNSUPPORTED,
                         "ratio 4 needs head_dim a multiple of 8 in [8, 8192] (got %d)", head_dim);
+    } else if (ratio == 128) {
+        if (head_dim % 64 != 0 || head_dim > 8192)
+            return fail(CSA_ERR_UNSUPPORTED,
+                        "ratio 128 needs head_dim a multiple of 64 in [64, 8192] (got %d)", head_dim);
     } else {
-        return fail(CSA_ERR_UNSUPPORTED, "ratio %d has no kernel (supported: 4)", ratio);
+        return fail(CSA_ERR_UNSUPPORTED, "ratio %d has no kernel (supported: 4, 128)", ratio);
     }
     if ((int64_t)capacity * head_dim >= kInt32Limit)
         return fail(CSA_ERR_TOO_LARGE, "capacity * head_dim = %lld does not fit int32 offsets",
@@ -201,7 +205,9 @@ int csa_compress_fwd(const void *kv, const void *score, const float *ape, const 
         return cuda_fail(e, "device set-up");
     csa::FwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim, capacity, out};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (csa::stream_supported(ratio, coff, head_dim))
+    if (csa::r128_supported(ratio, coff, head_dim))
+        e = csa::launch_fwd_r128(p, ds->status, st);
+    else if (csa::stream_supported(ratio, coff, head_dim))
         e = csa::launch_fwd_stream(p, csa::plan_stream(false, ratio, coff, head_dim, capacity, ds->num_sms),
                                    ds->status, st);
     else
@@ -239,11 +245,19 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
-    const bool streamed = csa::stream_supported(ratio, coff, head_dim);
+    const bool r128 = csa::r128_supported(ratio, coff, head_dim);
+    const bool streamed = !r128 && csa::stream_supported(ratio, coff, head_dim);
     csa::StreamPlan sp{};
     csa::SmallBwdPlan pl{};
     int64_t floats = 0;
-    if (streamed) {
+    int r128_blocks = 0;
+    if (r128) {
+        int partials = 0;
+        e = csa::r128_bwd_partials(coff, head_dim, capacity, &partials, &r128_blocks);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "backward plan");
+        floats = (int64_t)partials * ratio * coff * head_dim;
+    } else if (streamed) {
         sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, ds->num_sms);
         floats = (int64_t)csa::stream_bwd_partials(sp, capacity) * ratio * coff * head_dim;
     } else {
@@ -254,7 +268,9 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
     e = cudaMallocFromPoolAsync(&partial, (size_t)floats * sizeof(float), ds->pool, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward workspace");
-    if (streamed)
+    if (r128)
+        e = csa::launch_bwd_r128(p, static_cast<float *>(partial), r128_blocks, ds->status, st);
+    else if (streamed)
         e = csa::launch_bwd_stream(p, sp, static_cast<float *>(partial), ds->status, st);
     else
         e = csa::launch_bwd_small(p, pl, static_cast<float *>(partial), st);

@@ -79,6 +79,13 @@ cudaError_t launch_bwd_stream(const BwdParams &p, const StreamPlan &pl, float *p
 // The exact grid width launch_bwd_stream uses (partials = blocks / pl.cluster).
 cudaError_t stream_bwd_blocks(int ratio, int coff, const StreamPlan &pl, int capacity, int *blocks);
 
+// Ratio-128 family (chunked window, 2-D TMA staging), head_dim % 64 == 0.
+bool r128_supported(int ratio, int coff, int head_dim);
+cudaError_t launch_fwd_r128(const FwdParams &p, unsigned *status, cudaStream_t st);
+// grid width of the backward and the number of grad_ape partials it writes
+cudaError_t r128_bwd_partials(int coff, int head_dim, int capacity, int *partials, int *blocks);
+cudaError_t launch_bwd_r128(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st);
+
 // Records a status and the thread-local message returned by csa_last_error_message().
 int fail_status(int status, const char *fmt, ...);
 SmallBwdPlan plan_bwd_small(int ratio, int coff, int head_dim, int capacity, int num_sms);

@@ -6,7 +6,7 @@
 // step, a real-time loop in which growing or trimming a pool could block, or a
 // plug-in that is not allowed to touch the CUDA allocator at all.  This entry
 // point runs the same kernels with the scratch in a fixed array of this file
-// (kScratchFloats floats, 2 MiB) that lives in every GPU's memory from the moment
+// (kScratchFloats floats, 4 MiB) that lives in every GPU's memory from the moment
 // the library's device code is loaded until the process exits.  It calls no
 // cudaMalloc / cudaFree or allocating routine.
 //
@@ -23,9 +23,10 @@
 #include "csa.h"
 #include "csa_launch.h"
 
-// Scratch for the grad_ape partials: 524288 floats = 2 MiB per GPU.  Every
-// ratio-4 configuration needs less than half of it on a 152-SM GB300.
-static constexpr size_t kScratchFloats = 512u * 1024u;
+// Scratch for the grad_ape partials: 1048576 floats = 4 MiB per GPU.  Every
+// ratio-4 shape and the ratio-128 shapes with coff * head_dim up to 1024 fit on a
+// 152-SM GB300; wider ratio-128 shapes are rejected.
+static constexpr size_t kScratchFloats = 1024u * 1024u;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 // Status word of the bounded waits of calls made through this entry point.
 static __device__ __align__(256) unsigned g_noalloc_status[64];
@@ -114,11 +115,19 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
     csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool streamed = csa::stream_supported(ratio, coff, head_dim);
+    const bool r128 = csa::r128_supported(ratio, coff, head_dim);
+    const bool streamed = !r128 && csa::stream_supported(ratio, coff, head_dim);
     csa::StreamPlan sp{};
     csa::SmallBwdPlan pl{};
     int64_t floats = 0;
-    if (streamed) {
+    int r128_blocks = 0;
+    if (r128) {
+        int partials = 0;
+        e = csa::r128_bwd_partials(coff, head_dim, capacity, &partials, &r128_blocks);
+        if (e != cudaSuccess)
+            return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
+        floats = (int64_t)partials * ratio * coff * head_dim;
+    } else if (streamed) {
         sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, nd->num_sms);
         int blocks = 0;
         e = csa::stream_bwd_blocks(ratio, coff, sp, capacity, &blocks);
@@ -134,7 +143,9 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
                                 "csa_compress_bwd_noalloc needs %lld floats of grad_ape scratch for this shape; "
                                 "its fixed array holds %lld (use csa_compress_bwd)",
                                 (long long)floats, (long long)kScratchFloats);
-    if (streamed)
+    if (r128)
+        e = csa::launch_bwd_r128(p, nd->scratch, r128_blocks, nd->status, st);
+    else if (streamed)
         e = csa::launch_bwd_stream(p, sp, nd->scratch, nd->status, st);
     else
         e = csa::launch_bwd_small(p, pl, nd->scratch, st);

@@ -1,0 +1,777 @@
+// Compressor kernels for ratio 128 ("CSA Fused Compressor", cuDNN frontend docs,
+// sections Semantics and "ratio=128"): a window of 128 (coff 1) or 256 (coff 2)
+// tokens per output row -- too long for one thread -- is split into chunks of 8
+// window positions held by different threads and merged in a fixed order.
+//
+// Per thread block: a column tile of TC = 64 / coff columns, persistent over the
+// rows b, b + gridDim.x, ...  One producer warp streams, per row, the window's
+// [128 tokens x TC columns] boxes of kv and score (one box per array and part)
+// with 2-D TMA tensor copies into a shared-memory ring tracked by mbarriers (and,
+// in the backward, the grad_out row with a bulk copy).  Eight consumer warps: a
+// thread owns a group g of 4 columns and a chunk c of NC = 16*coff chunks, whose
+// window positions are k = c, c + NC, c + 2*NC, ... (8 of them), so that the
+// lanes of a warp read consecutive box rows (no bank conflicts) and each
+// thread's APE values stay in registers.
+//
+// Order of the arithmetic (the page's ratio-128 family: a deterministic chunked
+// order, checked against the plain sequential oracle by tolerance):
+//   s_k = score + ape;  m = max over all valid k (exact: chunk maxima, then the
+//   maximum of those);  e_k = exp(s_k - m) (the library's exp);
+//   den_c = ((+0 + e_c) + e_c+NC) + ... within chunk c, num_c = fma chain;
+//   den = ((+0 + den_0) + den_1) + ... over chunks ascending, num likewise;
+//   inv = rcp.rn(den);  o = num * inv;  out = bf16(o).
+// Backward per valid k: p = e_k * inv;  grad_kv = bf16(g*p);
+//   ds = p*(g*kv - g*o);  grad_score = bf16(ds); grad_ape as in the other kernels
+//   (per-thread sums over its rows, cluster merge in rank order, fixed-order
+//   finalisation).  Bitwise run-to-run deterministic: fixed chunks, fixed orders.
+//
+// Every barrier wait on the ring is bounded in time (timeouts are recorded in
+// the status word, the kernel then stops and exits normally).
+#include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "csa_device.cuh"
+#include "csa_launch.h"
+
+namespace cg = cooperative_groups;
+
+#ifndef CSA_R128_BWD_CLUSTER
+#define CSA_R128_BWD_CLUSTER 4
+#endif
+
+namespace csa {
+
+namespace {
+
+constexpr int kR = 128;  // ratio
+constexpr int kKC = 8;   // window positions per chunk (per thread)
+
+template <int COFF>
+struct Geo {
+    static constexpr int TC = 64 / COFF;      // columns per block tile
+    static constexpr int G = TC / 4;          // column groups (4 columns each)
+    static constexpr int CPW = 32 / G;        // chunks per warp
+    static constexpr int W = COFF * kR;       // window
+    static constexpr int NC = W / kKC;        // chunks
+    static constexpr int CW = NC / CPW;       // consumer warps (8)
+    static constexpr int CT = CW * 32;        // consumer threads
+    static constexpr int THREADS = CT + 32;   // + one producer warp
+    static constexpr int BOX_BYTES = kR * TC * 2;
+    static constexpr int WIN_BYTES = 2 * COFF * BOX_BYTES;
+};
+
+struct R128Args {
+    const uint16_t *kv;
+    const uint16_t *score;
+    const float *ape;
+    const int32_t *cu;
+    const int32_t *cc;
+    int n_seg;
+    int head_dim;
+    int capacity;
+    int stages;
+    int stage_bytes;
+    unsigned *status;
+};
+
+struct Meta {
+    int64_t base;
+    int seg;
+    int row;
+    int real;
+    int first;
+    int pad[2];
+};
+
+template <int COFF>
+struct R128Smem {
+    unsigned char *stages;
+    float *mx;   // [2][NC][TC]
+    float *den;  // [2][NC][TC]
+    float *num;  // [2][NC][TC]
+    float *fin;  // [2][2][TC]  (inv, g*o) for the backward
+    Meta *meta;
+    uint64_t *full;
+    uint64_t *empty;
+};
+
+template <int COFF>
+__host__ __device__ size_t r128_smem_bytes(int stages, int stage_bytes)
+{
+    using G = Geo<COFF>;
+    return (size_t)stages * stage_bytes + 3 * 2 * G::NC * G::TC * 4 + 2 * 2 * G::TC * 4 + sizeof(Meta) * stages +
+           16 * stages + 16;
+}
+
+template <int COFF>
+__device__ __forceinline__ R128Smem<COFF> r128_carve(unsigned char *base, int stages, int stage_bytes)
+{
+    using G = Geo<COFF>;
+    R128Smem<COFF> s;
+    s.stages = base;
+    unsigned char *p = base + (size_t)stages * stage_bytes;
+    s.mx = reinterpret_cast<float *>(p);
+    s.den = s.mx + 2 * G::NC * G::TC;
+    s.num = s.den + 2 * G::NC * G::TC;
+    s.fin = s.num + 2 * G::NC * G::TC;
+    p = reinterpret_cast<unsigned char *>(s.fin + 2 * 2 * G::TC);
+    s.meta = reinterpret_cast<Meta *>(p);
+    s.full = reinterpret_cast<uint64_t *>(s.meta + stages);
+    s.empty = s.full + stages;
+    return s;
+}
+
+// Box of array arr (0 kv, 1 score) and part p in a stage.
+template <int COFF>
+__device__ __forceinline__ int box_offset(int arr, int part)
+{
+    return (arr * COFF + part) * Geo<COFF>::BOX_BYTES;
+}
+
+// Window position k = c + NC*i of chunk c: its part and its token within the part.
+template <int COFF>
+__device__ __forceinline__ void position(int c, int i, int &part, int &tok)
+{
+    const int k = c + Geo<COFF>::NC * i;
+    part = k / kR;
+    tok = k - part * kR;
+}
+
+// ----------------------------------------------------------------- producer
+
+template <int COFF, bool BWD>
+__device__ void r128_produce(const R128Args &a, const R128Smem<COFF> &s, const CUtensorMap *tm_kv,
+                             const CUtensorMap *tm_sc, int c0, int row0, int rstride, int rend,
+                             const uint16_t *__restrict__ grad_out)
+{
+    using G = Geo<COFF>;
+    int issued = 0, st = 0;
+    uint32_t ph = 0;
+    for (int row = row0; row < rend; row += rstride) {
+        if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
+            break;
+        const RowMap rm = map_row(row, a.cu, a.cc, a.n_seg, kR);
+        Meta &m = s.meta[st];
+        m.base = rm.base;
+        m.seg = rm.seg;
+        m.row = row;
+        m.real = rm.real;
+        m.first = rm.first;
+        const bool load = BWD ? rm.real : true;
+        const int p0 = (COFF == 2 && rm.first) ? 1 : 0;
+        const uint32_t bytes =
+            load ? (uint32_t)((COFF - p0) * 2 * G::BOX_BYTES) + (BWD ? (uint32_t)G::TC * 2u : 0u) : 0u;
+        const uint32_t fb = smem_addr(&s.full[st]);
+        mbar_arrive_expect_tx(fb, bytes);
+        if (load) {
+            const uint32_t dst = smem_addr(s.stages + (size_t)st * a.stage_bytes);
+            for (int p = p0; p < COFF; ++p) {
+                const int y = (int)(rm.base + (int64_t)(p - (COFF - 1)) * kR);
+                const int x = p * a.head_dim + c0;
+                tma_load_2d(dst + box_offset<COFF>(0, p), tm_kv, x, y, fb);
+                tma_load_2d(dst + box_offset<COFF>(1, p), tm_sc, x, y, fb);
+            }
+            if (BWD)
+                bulk_g2s(dst + G::WIN_BYTES, grad_out + (int64_t)row * a.head_dim + c0, G::TC * 2, fb);
+        }
+        ++issued;
+        if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+    const int lo = issued > a.stages ? issued - a.stages : 0;
+    for (int it = lo; it < issued; ++it)
+        mbar_wait(smem_addr(&s.full[it % a.stages]), (uint32_t)(it / a.stages) & 1u, a.status);
+}
+
+// ----------------------------------------------------------------- consumer
+
+struct ChunkState {
+    uint2 kv[kKC];
+    float2 e[kKC][2];  // s_k, then e_k
+};
+
+template <int COFF>
+__device__ __forceinline__ bool pos_valid(int c, int i, bool first)
+{
+    int part, tok;
+    position<COFF>(c, i, part, tok);
+    return !(COFF == 2 && part == 0 && first);
+}
+
+template <int COFF>
+__device__ __forceinline__ void r128_load_ape(const R128Args &a, int c, int col, float2 (&ap)[kKC][2])
+{
+    const int64_t C = (int64_t)COFF * a.head_dim;
+#pragma unroll
+    for (int i = 0; i < kKC; ++i) {
+        int part, tok;
+        position<COFF>(c, i, part, tok);
+        const float4 v =
+            __ldg(reinterpret_cast<const float4 *>(a.ape + tok * C + (int64_t)part * a.head_dim + col));
+        ap[i][0] = make_float2(v.x, v.y);
+        ap[i][1] = make_float2(v.z, v.w);
+    }
+}
+
+// Reads the thread's positions of one row from the stage and forms s = score + ape.
+template <int COFF>
+__device__ __forceinline__ void r128_load(const unsigned char *stage, int c, int g, bool first,
+                                          const float2 (&ap)[kKC][2], ChunkState &cs)
+{
+#pragma unroll
+    for (int i = 0; i < kKC; ++i) {
+        if (!pos_valid<COFF>(c, i, first))
+            continue;
+        int part, tok;
+        position<COFF>(c, i, part, tok);
+        const int off = tok * Geo<COFF>::TC * 2 + 8 * g;
+        cs.kv[i] = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(0, part) + off);
+        const uint2 sw = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(1, part) + off);
+        cs.e[i][0] = add2(bf16x2_to_f2(sw.x), ap[i][0]);
+        cs.e[i][1] = add2(bf16x2_to_f2(sw.y), ap[i][1]);
+    }
+}
+
+// The two merge phases of one row.  Every consumer thread calls this once per
+// row.  The first barrier also votes on `ok` (the thread's wait for the row's
+// data succeeded): if any thread failed, all return false together before the
+// second barrier.  `have`: the row has data (cs loaded).  On true: cs.e holds e_k
+// of the thread's valid positions, and the chunk sums are in the merge buffers
+// for r128_merge.
+template <int COFF>
+__device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int c, int g, bool ok, bool have,
+                                          bool first, ChunkState &cs)
+{
+    using G = Geo<COFF>;
+    float2 m = make_float2(-INFINITY, -INFINITY), m2 = m;
+    if (have) {
+#pragma unroll
+        for (int i = 0; i < kKC; ++i) {
+            if (!pos_valid<COFF>(c, i, first))
+                continue;
+            m.x = max_nan(m.x, cs.e[i][0].x);
+            m.y = max_nan(m.y, cs.e[i][0].y);
+            m2.x = max_nan(m2.x, cs.e[i][1].x);
+            m2.y = max_nan(m2.y, cs.e[i][1].y);
+        }
+    }
+    float *mx = s.mx + (size_t)buf * G::NC * G::TC;
+    *reinterpret_cast<float4 *>(mx + c * G::TC + 4 * g) = make_float4(m.x, m.y, m2.x, m2.y);
+    if (!named_barrier_and(1, G::CT, ok))
+        return false;
+    float4 M = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+#pragma unroll 8
+    for (int cc = 0; cc < G::NC; ++cc) {
+        const float4 v = *reinterpret_cast<const float4 *>(mx + cc * G::TC + 4 * g);
+        M.x = max_nan(M.x, v.x);
+        M.y = max_nan(M.y, v.y);
+        M.z = max_nan(M.z, v.z);
+        M.w = max_nan(M.w, v.w);
+    }
+    float2 den[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    float2 num[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    const float2 negm[2] = {make_float2(-M.x, -M.y), make_float2(-M.z, -M.w)};
+#pragma unroll
+    for (int i = 0; i < kKC; ++i) {
+        if (!have || !pos_valid<COFF>(c, i, first))
+            continue;
+        const uint32_t kw[2] = {cs.kv[i].x, cs.kv[i].y};
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const float2 ek = exp2lanes(add2(cs.e[i][q], negm[q]));
+            cs.e[i][q] = ek;
+            den[q] = add2(den[q], ek);
+            num[q] = fma2(ek, bf16x2_to_f2(kw[q]), num[q]);
+        }
+    }
+    float *dn = s.den + (size_t)buf * G::NC * G::TC;
+    float *nm = s.num + (size_t)buf * G::NC * G::TC;
+    *reinterpret_cast<float4 *>(dn + c * G::TC + 4 * g) = make_float4(den[0].x, den[0].y, den[1].x, den[1].y);
+    *reinterpret_cast<float4 *>(nm + c * G::TC + 4 * g) = make_float4(num[0].x, num[0].y, num[1].x, num[1].y);
+    named_barrier(1, G::CT);
+    return true;
+}
+
+// The fixed-order chunk merge of tile column j: den and num.
+template <int COFF>
+__device__ __forceinline__ void r128_merge(const R128Smem<COFF> &s, int buf, int j, float &den, float &num)
+{
+    using G = Geo<COFF>;
+    const float *dn = s.den + (size_t)buf * G::NC * G::TC;
+    const float *nm = s.num + (size_t)buf * G::NC * G::TC;
+    den = 0.0f;
+    num = 0.0f;
+#pragma unroll 8
+    for (int cc = 0; cc < G::NC; ++cc) {
+        den = __fadd_rn(den, dn[cc * G::TC + j]);
+        num = __fadd_rn(num, nm[cc * G::TC + j]);
+    }
+}
+
+template <int COFF>
+__device__ __forceinline__ void r128_init(const R128Smem<COFF> &s, int stages)
+{
+    using G = Geo<COFF>;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(smem_addr(&s.full[i]), 1);
+            mbar_init(smem_addr(&s.empty[i]), G::CW);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ forward
+
+template <int COFF>
+__global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
+    fwd_r128_kernel(R128Args a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                    uint16_t *__restrict__ out)
+{
+    using G = Geo<COFF>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // TMA tensor destinations need 128-byte alignment: align the base by hand
+    // (the plan reserves 1 KB of slack for this).
+    unsigned char *smem_base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                                 ~uintptr_t(1023));
+    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes);
+    const int c0 = blockIdx.y * G::TC;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    r128_init<COFF>(s, a.stages);
+    if (warp == G::CW) {
+        if (lane == 0)
+            r128_produce<COFF, false>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
+        return;
+    }
+    const int g = lane % G::G, c = G::CPW * warp + lane / G::G;
+    float2 ap[kKC][2];
+    r128_load_ape<COFF>(a, c, c0 + 4 * g, ap);
+    int st = 0, buf = 0;
+    uint32_t ph = 0;
+    for (int row = blockIdx.x; row < a.capacity; row += gridDim.x) {
+        const bool ok = mbar_wait(smem_addr(&s.full[st]), ph, a.status);
+        const bool first = ok ? (bool)s.meta[st].first : true;
+        ChunkState cs;
+        if (ok)
+            r128_load<COFF>(s.stages + (size_t)st * a.stage_bytes, c, g, first, ap, cs);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&s.empty[st]));
+        if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
+        if (!r128_pool<COFF>(s, buf, c, g, ok, ok, first, cs))
+            break;
+        if (c < 4) {
+            const int j = 4 * g + c;
+            float den, num;
+            r128_merge<COFF>(s, buf, j, den, num);
+            const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, __frcp_rn(den)));
+            out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
+        }
+        buf ^= 1;
+    }
+}
+
+// ----------------------------------------------------------------- backward
+
+// Zero tokens [t0, t1) in the thread's 4 columns (first half only, or all halves);
+// the chunks share the tokens: thread chunk c takes t0 + c, t0 + c + NC, ...
+template <int COFF>
+__device__ __forceinline__ void r128_zero_tokens(uint16_t *dkv, uint16_t *dscore, int64_t C, int head_dim,
+                                                 int col, int64_t t0, int64_t t1, int64_t n_tokens, int c,
+                                                 bool all_halves)
+{
+    t1 = t1 < n_tokens ? t1 : n_tokens;
+    for (int64_t t = (t0 < 0 ? 0 : t0) + c; t < t1; t += Geo<COFF>::NC) {
+        *reinterpret_cast<uint2 *>(dkv + t * C + col) = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2 *>(dscore + t * C + col) = make_uint2(0u, 0u);
+        if (COFF == 2 && all_halves) {
+            *reinterpret_cast<uint2 *>(dkv + t * C + head_dim + col) = make_uint2(0u, 0u);
+            *reinterpret_cast<uint2 *>(dscore + t * C + head_dim + col) = make_uint2(0u, 0u);
+        }
+    }
+}
+
+template <int COFF>
+__global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
+    bwd_r128_kernel(R128Args a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                    int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
+                    uint16_t *__restrict__ dscore, float *__restrict__ partial)
+{
+    using G = Geo<COFF>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // TMA tensor destinations need 128-byte alignment: align the base by hand
+    // (the plan reserves 1 KB of slack for this).
+    unsigned char *smem_base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                                 ~uintptr_t(1023));
+    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes);
+    const int c0 = blockIdx.y * G::TC;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t C = (int64_t)COFF * a.head_dim;
+    const int R = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;
+    const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
+    const int rend = R < a.capacity ? R : a.capacity;
+    const int64_t n_tokens = n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg);
+    asm volatile("griddepcontrol.launch_dependents;");
+    r128_init<COFF>(s, a.stages);
+
+    const int g = lane % G::G, c = G::CPW * warp + lane / G::G;
+    const int col = c0 + 4 * g;  // thread's first column within a half
+    float2 acc[kKC][2];
+#pragma unroll
+    for (int i = 0; i < kKC; ++i)
+        acc[i][0] = acc[i][1] = make_float2(0.0f, 0.0f);
+
+    if (warp == G::CW) {
+        if (lane == 0)
+            r128_produce<COFF, true>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, rend, grad_out);
+    } else {
+        if (blockIdx.x == 0) {  // leading gap: tokens before the first real block
+            int64_t lead = n_tokens;
+            if (R0 < R)
+                lead = map_row(R0, a.cu, a.cc, a.n_seg, kR).base;
+            r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, 0, lead, n_tokens, c, true);
+        }
+        float2 ap[kKC][2];
+        r128_load_ape<COFF>(a, c, col, ap);
+        int st = 0, buf = 0;
+        uint32_t ph = 0;
+        for (int row = blockIdx.x; row < rend; row += gridDim.x) {
+            const bool ok = mbar_wait(smem_addr(&s.full[st]), ph, a.status);
+            Meta m = Meta{0, 0, row, 0, 1, {0, 0}};
+            if (ok)
+                m = s.meta[st];
+            // rows below cu_seqlens_comp[0] are not real: no loads, no gradient
+            const bool first = m.first || !m.real;
+            const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
+            ChunkState cs;
+            if (ok && m.real)
+                r128_load<COFF>(stage, c, g, first, ap, cs);
+            uint2 gw = make_uint2(0u, 0u);
+            if (ok && m.real)
+                gw = *reinterpret_cast<const uint2 *>(stage + G::WIN_BYTES + 8 * g);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&s.empty[st]));
+            if (++st == a.stages) {
+                st = 0;
+                ph ^= 1u;
+            }
+            if (!r128_pool<COFF>(s, buf, c, g, ok, ok && m.real, first, cs))
+                break;
+            const float2 gg[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
+            float *fin = s.fin + (size_t)buf * 2 * G::TC;
+            if (c < 4) {
+                const int j = 4 * g + c;
+                float den, num;
+                r128_merge<COFF>(s, buf, j, den, num);
+                const float inv = __frcp_rn(den);
+                const float gj = c == 0 ? gg[0].x : c == 1 ? gg[0].y : c == 2 ? gg[1].x : gg[1].y;
+                fin[j] = inv;
+                fin[G::TC + j] = __fmul_rn(gj, __fmul_rn(num, inv));
+            }
+            named_barrier(1, G::CT);
+            buf ^= 1;
+            if (!m.real)
+                continue;
+            const float4 inv4 = *reinterpret_cast<const float4 *>(fin + 4 * g);
+            const float4 go4 = *reinterpret_cast<const float4 *>(fin + G::TC + 4 * g);
+            const float2 inv[2] = {make_float2(inv4.x, inv4.y), make_float2(inv4.z, inv4.w)};
+            const float2 ngo[2] = {make_float2(-go4.x, -go4.y), make_float2(-go4.z, -go4.w)};
+#pragma unroll
+            for (int i = 0; i < kKC; ++i) {
+                if (!pos_valid<COFF>(c, i, first))
+                    continue;
+                int part, tk;
+                position<COFF>(c, i, part, tk);
+                const uint32_t kw[2] = {cs.kv[i].x, cs.kv[i].y};
+                uint32_t dk[2], dsw[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float2 pk = mul2(cs.e[i][q], inv[q]);
+                    dk[q] = f2_to_bf16x2(mul2(gg[q], pk));
+                    const float2 ds = mul2(pk, add2(mul2(gg[q], bf16x2_to_f2(kw[q])), ngo[q]));
+                    dsw[q] = f2_to_bf16x2(ds);
+                    acc[i][q] = add2(acc[i][q], ds);
+                }
+                const int64_t tok = m.base + (int64_t)(part - (COFF - 1)) * kR + tk;
+                if (tok < n_tokens) {
+                    const int64_t gi = tok * C + (int64_t)part * a.head_dim + col;
+                    *reinterpret_cast<uint2 *>(dkv + gi) = make_uint2(dk[0], dk[1]);
+                    *reinterpret_cast<uint2 *>(dscore + gi) = make_uint2(dsw[0], dsw[1]);
+                }
+            }
+            if (m.row + 1 == __ldg(a.cc + m.seg + 1)) {  // last block of its segment
+                if (COFF == 2)  // own block's first-half columns: read by no row
+                    r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, m.base, m.base + kR, n_tokens, c, false);
+                int64_t next = n_tokens;
+                if (m.row + 1 < R)
+                    next = map_row(m.row + 1, a.cu, a.cc, a.n_seg, kR).base;
+                r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, m.base + kR, next, n_tokens, c, true);
+            }
+        }
+    }
+    __syncthreads();  // the ring is idle: its stages become the grad_ape staging area
+    // grad_ape partial [ape row][part][tile column]
+    float *red = reinterpret_cast<float *>(s.stages);
+    if (warp < G::CW) {
+#pragma unroll
+        for (int i = 0; i < kKC; ++i) {
+            int part, tk;
+            position<COFF>(c, i, part, tk);
+            *reinterpret_cast<float4 *>(red + (tk * COFF + part) * G::TC + 4 * g) =
+                make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
+        }
+    }
+    __syncthreads();
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int rank = (int)cluster.block_rank();
+    const int nrank = (int)cluster.num_blocks();
+    const int n4 = kR * COFF * G::TC / 4;
+    const int share = (n4 + nrank - 1) / nrank;
+    const int lo = rank * share, hi = lo + share < n4 ? lo + share : n4;
+    float *dst = partial + (int64_t)(blockIdx.x / nrank) * kR * C;
+    for (int i4 = lo + (int)threadIdx.x; i4 < hi; i4 += blockDim.x) {
+        const int rp = (i4 * 4) / G::TC, lcol = i4 * 4 - rp * G::TC;
+        const int arow = rp / COFF, pp = rp - arow * COFF;
+        float4 v4 = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(red, 0) + i4 * 4);
+        for (int q = 1; q < nrank; ++q) {
+            const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(red, q) + i4 * 4);
+            v4.x = __fadd_rn(v4.x, v.x);
+            v4.y = __fadd_rn(v4.y, v.y);
+            v4.z = __fadd_rn(v4.z, v.z);
+            v4.w = __fadd_rn(v4.w, v.w);
+        }
+        *reinterpret_cast<float4 *>(dst + (int64_t)arow * C + (int64_t)pp * a.head_dim + c0 + lcol) = v4;
+    }
+    cluster.sync();
+}
+
+// ------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t *err)
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static cudaError_t e = cudaSuccess;
+    std::call_once(once, []() {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            e = cudaErrorNotSupported;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    *err = e;
+    return fn;
+}
+
+// Tensor map of a [rows, C] bf16 row-major tensor with [128 x tc] boxes.  The row
+// extent is the int32 flat-offset bound, not the (unknown to the forward) token
+// count: every box the kernels request lies inside a real block.
+cudaError_t make_map(CUtensorMap *m, const void *ptr, int64_t C, int tc)
+{
+    cudaError_t e;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn(&e);
+    if (e != cudaSuccess)
+        return e;
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(((int64_t)1 << 31) / C)};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)tc, (cuuint32_t)kR};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+struct R128Plan {
+    int stages, stage_bytes, threads, tiles, cluster;
+    size_t smem;
+};
+
+template <int COFF>
+R128Plan r128_plan(bool bwd, int head_dim)
+{
+    using G = Geo<COFF>;
+    R128Plan pl;
+    pl.stage_bytes = (G::WIN_BYTES + (bwd ? G::TC * 2 : 0) + 1023) / 1024 * 1024;
+    pl.stages = 2;
+    pl.threads = G::THREADS;
+    pl.tiles = head_dim / G::TC;
+    pl.cluster = bwd ? CSA_R128_BWD_CLUSTER : 1;
+    pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes) + 1024;  // + alignment slack
+    if (bwd) {  // grad_ape staging reuses the stages: make sure it fits
+        const size_t red = (size_t)kR * COFF * G::TC * sizeof(float);
+        if ((size_t)pl.stages * pl.stage_bytes < red)
+            pl.stages = (int)((red + pl.stage_bytes - 1) / pl.stage_bytes);
+        pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes) + 1024;
+    }
+    return pl;
+}
+
+template <int COFF>
+cudaError_t r128_blocks(const R128Plan &pl, bool bwd, int rows, int *out)
+{
+    const void *fn = bwd ? reinterpret_cast<const void *>(bwd_r128_kernel<COFF>)
+                         : reinterpret_cast<const void *>(fwd_r128_kernel<COFF>);
+    static std::mutex mu;
+    static int cache_dev[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    static int cache_val[8];
+    static const void *cache_fn[8];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    int resident = -1;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < 8; ++i)
+            if (cache_dev[i] == dev && cache_fn[i] == fn)
+                resident = cache_val[i];
+    }
+    if (resident < 0) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        if (e != cudaSuccess)
+            return e;
+        if (pl.cluster > 1) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(pl.cluster, 1, 1);
+            cfg.blockDim = dim3(pl.threads, 1, 1);
+            cfg.dynamicSmemBytes = pl.smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = pl.cluster;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            e = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
+            resident = clusters * pl.cluster;
+        } else {
+            int per_sm = 0, sms = 0;
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, pl.threads, pl.smem);
+            if (e == cudaSuccess)
+                e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            resident = per_sm * sms;
+        }
+        if (e != cudaSuccess)
+            return e;
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < 8; ++i)
+            if (cache_dev[i] < 0) {
+                cache_dev[i] = dev;
+                cache_fn[i] = fn;
+                cache_val[i] = resident;
+                break;
+            }
+    }
+    int blocks = (resident > 0 ? resident : 1) / pl.tiles;
+    blocks = blocks / pl.cluster * pl.cluster;
+    if (blocks < pl.cluster)
+        blocks = pl.cluster;
+    const int need = rows > 0 ? rows : 1;
+    if (blocks > need)
+        blocks = (need + pl.cluster - 1) / pl.cluster * pl.cluster;
+    *out = blocks;
+    return cudaSuccess;
+}
+
+template <int COFF>
+cudaError_t launch_fwd_r128_t(const FwdParams &p, unsigned *status, cudaStream_t st)
+{
+    const R128Plan pl = r128_plan<COFF>(false, p.head_dim);
+    int blocks = 0;
+    cudaError_t e = r128_blocks<COFF>(pl, false, p.capacity, &blocks);
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap mk, ms;
+    const int64_t C = (int64_t)COFF * p.head_dim;
+    if ((e = make_map(&mk, p.kv, C, Geo<COFF>::TC)) != cudaSuccess ||
+        (e = make_map(&ms, p.score, C, Geo<COFF>::TC)) != cudaSuccess)
+        return e;
+    R128Args a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
+               p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes, status};
+    fwd_r128_kernel<COFF><<<dim3(blocks, pl.tiles), pl.threads, pl.smem, st>>>(a, mk, ms,
+                                                                              static_cast<uint16_t *>(p.out));
+    return cudaGetLastError();
+}
+
+template <int COFF>
+cudaError_t r128_bwd_blocks_t(int head_dim, int capacity, int *blocks)
+{
+    const R128Plan pl = r128_plan<COFF>(true, head_dim);
+    return r128_blocks<COFF>(pl, true, capacity, blocks);
+}
+
+template <int COFF>
+cudaError_t launch_bwd_r128_t(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st)
+{
+    const R128Plan pl = r128_plan<COFF>(true, p.head_dim);
+    CUtensorMap mk, ms;
+    const int64_t C = (int64_t)COFF * p.head_dim;
+    cudaError_t e;
+    if ((e = make_map(&mk, p.kv, C, Geo<COFF>::TC)) != cudaSuccess ||
+        (e = make_map(&ms, p.score, C, Geo<COFF>::TC)) != cudaSuccess)
+        return e;
+    R128Args a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
+               p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes, status};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, pl.tiles, 1);
+    cfg.blockDim = dim3(pl.threads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_r128_kernel<COFF>, a, mk, ms, p.n_tokens,
+                           static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
+                           static_cast<uint16_t *>(p.dscore), partial);
+    if (e != cudaSuccess)
+        return e;
+    return launch_dape_finalize(partial, blocks / pl.cluster, (int64_t)kR * C, p.dape, st);
+}
+
+}  // namespace
+
+bool r128_supported(int ratio, int coff, int head_dim)
+{
+    return ratio == kR && (coff == 1 || coff == 2) && head_dim % 64 == 0 && head_dim <= 8192;
+}
+
+cudaError_t launch_fwd_r128(const FwdParams &p, unsigned *status, cudaStream_t st)
+{
+    return p.coff == 2 ? launch_fwd_r128_t<2>(p, status, st) : launch_fwd_r128_t<1>(p, status, st);
+}
+
+// grad_ape partials the backward will write (the workspace needs that many
+// ratio x coff*head_dim slabs); also the grid width it will use.
+cudaError_t r128_bwd_partials(int coff, int head_dim, int capacity, int *partials, int *blocks)
+{
+    cudaError_t e = coff == 2 ? r128_bwd_blocks_t<2>(head_dim, capacity, blocks)
+                              : r128_bwd_blocks_t<1>(head_dim, capacity, blocks);
+    *partials = *blocks / CSA_R128_BWD_CLUSTER;
+    return e;
+}
+
+cudaError_t launch_bwd_r128(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st)
+{
+    return p.coff == 2 ? launch_bwd_r128_t<2>(p, partial, blocks, status, st)
+                       : launch_bwd_r128_t<1>(p, partial, blocks, status, st);
+}
+
+}  // namespace csa

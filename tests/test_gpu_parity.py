@@ -206,3 +206,85 @@ def test_both_kernel_families_agree_bitwise(csa):
 def test_zz_no_bounded_wait_expired(csa):
     """No kernel of this module recorded a timeout in the device status word."""
     assert csa.csa_device_status(clear=True) == 0
+
+
+# ------------------------------------------------------------ ratio 128 family
+
+def fp64_parity_ok(got_bits, ref32_bits, ref64):
+    """fp64-oracle parity ("CSA Fused Compressor", Numerics): the kernel is at least
+    as close to the fp64 oracle as the plain fp32 evaluation:
+    err_gpu <= err_fp32 * (1 + 1e-6) + 1e-4, err = max |bf16 value - fp64|."""
+    err_gpu = np.abs(F(got_bits).astype(np.float64) - ref64).max()
+    err_32 = np.abs(F(ref32_bits).astype(np.float64) - ref64).max()
+    return err_gpu <= err_32 * (1 + 1e-6) + 1e-4
+
+
+def tolerance_counts(c, csa, scale=1.0):
+    """The ratio-128 contract ("CSA Fused Compressor", Numerics: ratio == 128),
+    per case: no NaN, max_abs <= 1.6e-2 against the plain fp32 and the fp64
+    oracle, fp64 parity no worse than the plain fp32 evaluation, never-consumed
+    slots exact zeros, grad_ape within 1e-5 (normwise) of fp64.  Returns the outputs and the
+    (differing-from-fp32, differing-from-fp64, size) counts of out / grad_kv /
+    grad_score, whose max(1, 0.1%) bound the callers apply."""
+    d = Dev(c)
+    out = run_fwd(d, csa)
+    dkv, dsc, dape = run_bwd(d, csa)
+    ref32 = (oracle.case_fwd_f32(c),) + tuple(oracle.case_bwd_f32(c))
+    ref64 = (oracle.case_fwd_f64(c),) + tuple(oracle.case_bwd_f64(c))
+    counts = []
+    for got, r32, r64, bound in ((out, ref32[0], ref64[0], 1.6e-2 * scale),
+                                 (dkv, ref32[1], ref64[1], 1.6e-2 * scale),
+                                 (dsc, ref32[2], ref64[2], 1.6e-2 * scale * scale)):
+        assert not np.isnan(F(got)).any()
+        assert np.abs(F(got).astype(np.float64) - F(r32)).max() <= bound
+        n64, max_abs = tolerance_report(got, r64)
+        assert max_abs <= bound
+        assert fp64_parity_ok(got, r32, r64)
+        counts.append((int((got != r32).sum()), n64, got.size))
+    owner = oracle.consumers(c.cu_seqlens, c.cu_seqlens_comp, c.ratio, c.coff, c.head_dim, c.capacity, c.n_tokens)
+    unread = owner == -1
+    assert not dkv[unread].any() and not dsc[unread].any()
+    assert np.abs(dape - ref64[3]).max() <= 1e-5 * np.abs(ref64[3]).max()
+    return (out, dkv, dsc, dape), counts
+
+
+def assert_counts(counts):
+    for n32, n64, size in counts:
+        assert n32 <= max(1, 0.001 * size), (n32, size)
+        assert n64 <= max(1, 0.001 * size), (n64, size)
+
+
+def test_r128_workload_tolerance_and_determinism(csa):
+    c = w.WORKLOADS["r128c1d512_4x32768"]()
+    (out, dkv, dsc, dape), counts = tolerance_counts(c, csa)
+    assert_counts(counts)
+    d = Dev(c)
+    assert np.array_equal(run_fwd(d, csa, canary=0x7FC1), out)
+    b = run_bwd(d, csa, canary=0x7FC1, dape_fill=7.0)
+    assert np.array_equal(b[0], dkv) and np.array_equal(b[1], dsc)
+    assert np.array_equal(b[2].view(np.uint32), dape.view(np.uint32))
+
+
+R128_LAYOUTS = [[2400, 128, 5, 8000], [127], [128], [129, 0, 2048], [5120], [3, 5600, 2]]
+
+
+@pytest.mark.parametrize("coff", [1, 2])
+@pytest.mark.parametrize("head_dim", [64, 128, 192])
+def test_r128_small_layouts(csa, coff, head_dim):
+    """Ragged ratio-128 packs (segments shorter than ratio, tails, empty segments,
+    padding rows, token padding): per-case checks, and the differing-element
+    bound over the union of the cases (each case is too small for a 0.1% bound)."""
+    total = [[0, 0, 0] for _ in range(3)]
+    for li, lens in enumerate(R128_LAYOUTS):
+        T = sum(lens) + (0, 7)[li % 2]
+        R = sum(L // 128 for L in lens)
+        extra = (0, 2, 1)[li % 3]
+        if (T < 128 and R + extra > 0) or R + extra == 0:
+            continue
+        c = w.make_case("r128lay", 128, coff, head_dim, lens, extra_rows=extra, n_tokens=T, seed=li + 40)
+        _, counts = tolerance_counts(c, csa)
+        for t, (a, b, n) in zip(total, counts):
+            t[0] += a
+            t[1] += b
+            t[2] += n
+    assert_counts([tuple(t) for t in total])

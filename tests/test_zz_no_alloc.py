@@ -63,3 +63,31 @@ def test_noalloc_rejects_bad_arguments_before_launch(csa):
     assert ei.value.status == 3  # misaligned dape
     torch.cuda.synchronize()
     assert not dkv.any()
+
+
+def test_noalloc_ratio128_matches_backward(csa):
+    c = w.make_case("na128", 128, 1, 512, [4096, 300], extra_rows=3, seed=5)
+    d = Dev(c)
+    want = run_bwd(d, csa)
+    for canary in (0xFFFF, 0x7FC1):
+        got = run_noalloc(d, csa, canary)
+        assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
+        assert np.abs(got[2] - want[2]).max() <= 1e-5 * np.abs(want[2]).max()
+
+
+def test_noalloc_rejects_shape_beyond_its_scratch(csa):
+    """ratio 128, coff 2, head_dim 8192: one grad_ape partial is 128 x 16384 floats
+    (8 MiB), more than the fixed array holds: rejected before launch."""
+    import torch
+    c = w.make_case("na_big", 128, 2, 8192, [256], seed=6)
+    d = Dev(c)
+    C = 2 * 8192
+    dkv = torch.zeros((c.n_tokens, C), dtype=torch.int16, device="cuda")
+    dape = torch.zeros((128, C), dtype=torch.float32, device="cuda")
+    with pytest.raises(csa.CSAError) as ei:
+        csa.csa_compress_bwd_noalloc(d.kv, d.score, d.ape, d.cu, d.cc, c.n_seg, 128, 2, 8192, c.capacity,
+                                     c.n_tokens, d.g, dkv, dkv, dape)
+    assert ei.value.status == 4  # CSA_ERR_TOO_LARGE
+    assert "scratch" in str(ei.value)
+    torch.cuda.synchronize()
+    assert not dkv.any()
