@@ -135,6 +135,19 @@ class ClockSampler:
 
 # ------------------------------------------------------------ our arm
 
+def max_over_ranks(values):
+    """Element-wise max of a list of floats over all ranks of the default process
+    group (NCCL on GPUs, gloo on CPU), or the list itself with no group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor(list(values), dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def measured_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -237,10 +250,7 @@ def run_ours(args, rank, world, local_rank):
     t_bwd = [e[2].elapsed_time(e[3]) for e in evs]
     ms_fwd, ms_bwd = sum(t_fwd) / len(t_fwd), sum(t_bwd) / len(t_bwd)
     ms_step = ms_fwd + ms_bwd
-    if world > 1:
-        t = torch.tensor([ms_step, ms_fwd, ms_bwd], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_fwd, ms_bwd = [float(x) for x in t.cpu()]
+    ms_step, ms_fwd, ms_bwd = max_over_ranks([ms_step, ms_fwd, ms_bwd])
 
     e2e = None if args.no_e2e else run_e2e(args, c, csa, dev, stream, world)
     return c, ms_step, ms_fwd, ms_bwd, clocks, e2e
@@ -288,12 +298,7 @@ def run_e2e(args, c, csa, dev, stream, world):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / k
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks([e0.elapsed_time(e1) / k])[0]
     return {"value": world * c.n_tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 

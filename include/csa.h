@@ -177,6 +177,16 @@ CSA_API const char *csa_last_error_message(void);
  */
 CSA_API int csa_device_status(int clear);
 
+/*
+ * Self-test of the bounded waits (failure detection without a GPU fault): launches
+ * one small kernel on `stream` that waits on a shared-memory barrier phase nothing
+ * completes, giving up after limit_ns (at most 1e9) and recording a timeout in the
+ * device status word exactly as the pipelined kernels would.  The kernel then
+ * exits normally and the context stays usable; csa_device_status() afterwards
+ * returns CSA_ERR_DEVICE_TIMEOUT (clear it with csa_device_status(1)).
+ */
+CSA_API int csa_selftest_bounded_wait(int64_t limit_ns, void *stream);
+
 /* Library version as an integer: major * 10000 + minor * 100 + patch. */
 CSA_API int csa_version(void);
 

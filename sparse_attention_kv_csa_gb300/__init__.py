@@ -30,7 +30,7 @@ from . import _build
 
 __all__ = [
     "csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support", "csa_status_string",
-    "csa_last_error_message", "csa_version", "csa_device_status", "CSAError", "compress_forward", "compress_backward",
+    "csa_last_error_message", "csa_version", "csa_device_status", "csa_selftest_bounded_wait", "CSAError", "compress_forward", "compress_backward",
     "library_path", "STATUS",
 ]
 
@@ -56,12 +56,13 @@ def _load():
     lib.csa_compress_bwd_noalloc.argtypes = common + [i64, P, P, P, P, P]
     lib.csa_check_support.argtypes = [i32, i32, i32, i64, i32]
     lib.csa_device_status.argtypes = [ctypes.c_int]
+    lib.csa_selftest_bounded_wait.argtypes = [i64, P]
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_last_error_message.argtypes = []
     lib.csa_last_error_message.restype = ctypes.c_char_p
     for f in ("csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support",
-              "csa_version", "csa_device_status"):
+              "csa_version", "csa_device_status", "csa_selftest_bounded_wait"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -110,6 +111,11 @@ def csa_version() -> int:
 def csa_device_status(clear: bool = False) -> int:
     """Synchronises and returns the device status (0 = no bounded wait expired)."""
     return _lib.csa_device_status(1 if clear else 0)
+
+
+def csa_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Launches the bounded-wait self-test kernel (see csa.h)."""
+    _check(_lib.csa_selftest_bounded_wait(limit_ns, _stream(stream)))
 
 
 def csa_check_support(ratio, coff, head_dim, n_tokens, capacity) -> int:

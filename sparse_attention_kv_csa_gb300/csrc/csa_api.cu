@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "csa.h"
+#include "csa_device.cuh"
 #include "csa_launch.h"
 
 namespace {
@@ -279,6 +280,39 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
         return cuda_fail(e, "backward launch");
     if (e2 != cudaSuccess)
         return cuda_fail(e2, "backward workspace release");
+    return CSA_OK;
+}
+
+namespace {
+
+// Waits for a phase of a shared-memory barrier that nothing ever completes: the
+// bounded wait must give up after limit_ns and record a timeout.
+__global__ void selftest_wait_kernel(unsigned *status, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        csa::mbar_init(csa::smem_addr(&bar), 1);
+        csa::mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        csa::mbar_wait(csa::smem_addr(&bar), 0u, status, limit_ns);
+}
+
+}  // namespace
+
+int csa_selftest_bounded_wait(int64_t limit_ns, void *stream)
+{
+    if (limit_ns < 0 || limit_ns > 1000000000ll)
+        return fail(CSA_ERR_INVALID_VALUE, "limit_ns must be in [0, 1e9] (got %lld)", (long long)limit_ns);
+    DeviceState *ds = nullptr;
+    cudaError_t e = device_state(&ds);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device set-up");
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ds->status, (uint64_t)limit_ns);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "self-test launch");
     return CSA_OK;
 }
 

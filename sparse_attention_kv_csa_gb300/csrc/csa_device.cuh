@@ -202,7 +202,8 @@ constexpr unsigned kStatusTimeout = 1u;
 // *status and returns false; the caller then stops its loop instead of hanging.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *status,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -210,7 +211,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     for (uint32_t it = 1; it < (1u << 28); ++it) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs)
+        if ((it & 255u) == 0 && global_ns() - t0 > limit_ns)
             break;
     }
     atomicCAS(status, 0u, kStatusTimeout);
