@@ -187,6 +187,18 @@ CSA_API int csa_device_status(int clear);
  */
 CSA_API int csa_selftest_bounded_wait(int64_t limit_ns, void *stream);
 
+/*
+ * Self-test of the reciprocal the kernels take of each softmax denominator (the
+ * pages have no counterpart: they only fix fp32 arithmetic).  Writes, for i < n,
+ * out[i] = the library's 1/d[i]; that routine is correctly rounded for d in
+ * [1, 256], the range every denominator falls in (NaN in, NaN out), and is
+ * unspecified elsewhere.  d and out are device pointers to n floats, 4-byte
+ * aligned, not overlapping; n >= 0 (n == 0 launches nothing).  Asynchronous on
+ * `stream`.  Returns CSA_ERR_INVALID_VALUE for a NULL pointer with n > 0 or for
+ * n < 0, CSA_ERR_CUDA when the launch fails.
+ */
+CSA_API int csa_selftest_reciprocal(const float *d, float *out, int64_t n, void *stream);
+
 /* Library version as an integer: major * 10000 + minor * 100 + patch. */
 CSA_API int csa_version(void);
 

@@ -30,7 +30,8 @@ from . import _build
 
 __all__ = [
     "csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support", "csa_status_string",
-    "csa_last_error_message", "csa_version", "csa_device_status", "csa_selftest_bounded_wait", "CSAError", "compress_forward", "compress_backward",
+    "csa_last_error_message", "csa_version", "csa_device_status", "csa_selftest_bounded_wait",
+    "csa_selftest_reciprocal", "CSAError", "compress_forward", "compress_backward",
     "library_path", "STATUS",
 ]
 
@@ -57,12 +58,13 @@ def _load():
     lib.csa_check_support.argtypes = [i32, i32, i32, i64, i32]
     lib.csa_device_status.argtypes = [ctypes.c_int]
     lib.csa_selftest_bounded_wait.argtypes = [i64, P]
+    lib.csa_selftest_reciprocal.argtypes = [P, P, i64, P]
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_last_error_message.argtypes = []
     lib.csa_last_error_message.restype = ctypes.c_char_p
     for f in ("csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support",
-              "csa_version", "csa_device_status", "csa_selftest_bounded_wait"):
+              "csa_version", "csa_device_status", "csa_selftest_bounded_wait", "csa_selftest_reciprocal"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -116,6 +118,11 @@ def csa_device_status(clear: bool = False) -> int:
 def csa_selftest_bounded_wait(limit_ns: int, stream=None) -> None:
     """Launches the bounded-wait self-test kernel (see csa.h)."""
     _check(_lib.csa_selftest_bounded_wait(limit_ns, _stream(stream)))
+
+
+def csa_selftest_reciprocal(d, out, n: int, stream=None) -> None:
+    """The kernels' denominator reciprocal applied to n device floats (see csa.h)."""
+    _check(_lib.csa_selftest_reciprocal(_addr(d), _addr(out), n, _stream(stream)))
 
 
 def csa_check_support(ratio, coff, head_dim, n_tokens, capacity) -> int:

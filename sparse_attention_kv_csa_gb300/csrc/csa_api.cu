@@ -299,7 +299,34 @@ __global__ void selftest_wait_kernel(unsigned *status, uint64_t limit_ns)
         csa::mbar_wait(csa::smem_addr(&bar), 0u, status, limit_ns);
 }
 
+__global__ void selftest_recip_kernel(const float *__restrict__ d, float *__restrict__ out, int64_t n)
+{
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = csa::recip_den(d[i]);
+}
+
 }  // namespace
+
+int csa_selftest_reciprocal(const float *d, float *out, int64_t n, void *stream)
+{
+    if (n < 0)
+        return fail(CSA_ERR_INVALID_VALUE, "n must be >= 0 (got %lld)", (long long)n);
+    if (n == 0)
+        return CSA_OK;
+    if (!d || !out)
+        return fail(CSA_ERR_INVALID_VALUE, "d and out must not be NULL");
+    DeviceState *ds = nullptr;
+    cudaError_t e = device_state(&ds);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device set-up");
+    const int64_t want = (n + 255) / 256;
+    const int blocks = (int)(want < 8 * (int64_t)ds->num_sms ? want : 8 * (int64_t)ds->num_sms);
+    selftest_recip_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(d, out, n);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, "self-test launch");
+    return CSA_OK;
+}
 
 int csa_selftest_bounded_wait(int64_t limit_ns, void *stream)
 {

@@ -5,7 +5,8 @@
 // window arithmetic is fp32 with one final bf16 rounding, and every add, multiply
 // and fused multiply-add is an explicit round-to-nearest instruction, so nothing
 // depends on the compiler contracting a*b+c.  The library is built without
-// --use_fast_math: no flush-to-zero, IEEE division and reciprocal.
+// --use_fast_math: no flush-to-zero; the one reciprocal per output (recip_den)
+// is correctly rounded.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -29,6 +30,28 @@ __device__ __forceinline__ float max_nan(float a, float b)
     float d;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
     return d;
+}
+
+// ----------------------------------------------------------- reciprocal
+// 1/d rounded to nearest for d in [1, 256]: the range of a softmax denominator
+// whose largest term is exactly 1 and which has at most 256 terms (NaN stays NaN).
+// Seed: the hardware approximation rcp.approx, within one ulp of 1/d by the PTX
+// ISA.  One Newton-Raphson correction in Markstein's fused form (P. Markstein,
+// IBM J. Res. Dev. 34(1), 1990): the residual r = 1 - d*y is exact in one FMA, and
+// y + y*r rounded once is the correctly rounded 1/d for every seed within one ulp,
+// except when the significand of d is all ones, d = 2^k (2 - 2^-23).  There 1/d
+// lies just above a rounding tie, the seed 2^(-k-1) lands on the tie, and the
+// correctly rounded result 2^(-k-1) (1 + 2^-23) is the step's result with its
+// lowest bit set.  Both statements hold exhaustively over one binade, and the step
+// commutes with scaling by a power of two on this range.
+__device__ __forceinline__ float recip_den(float d)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
+    const float r = __fmaf_rn(-d, y, 1.0f);
+    const uint32_t b = __float_as_uint(__fmaf_rn(y, r, y));
+    const uint32_t tie = (~__float_as_uint(d) & 0x7fffffu) == 0u ? 1u : 0u;
+    return __uint_as_float(b | tie);
 }
 
 // ------------------------------------------------------------------ exp

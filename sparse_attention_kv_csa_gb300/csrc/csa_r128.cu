@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
             const int j = 4 * g + c;
             float den, num;
             r128_merge<COFF>(s, buf, j, den, num);
-            const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, __frcp_rn(den)));
+            const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, recip_den(den)));
             out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
         }
         buf ^= 1;
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
                 const int j = 4 * g + c;
                 float den, num;
                 r128_merge<COFF>(s, buf, j, den, num);
-                const float inv = __frcp_rn(den);
+                const float inv = recip_den(den);
                 const float gj = c == 0 ? gg[0].x : c == 1 ? gg[0].y : c == 2 ? gg[1].x : gg[1].y;
                 fin[j] = inv;
                 fin[G::TC + j] = __fmul_rn(gj, __fmul_rn(num, inv));

@@ -252,7 +252,7 @@ __device__ __forceinline__ void fwd_compute(const SmallArgs &a, const FwdUnit<RA
     uint32_t o[NW];
 #pragma unroll
     for (int q = 0; q < NW; ++q) {
-        const float2 inv = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
+        const float2 inv = make_float2(recip_den(den[q].x), recip_den(den[q].y));
         o[q] = f2_to_bf16x2(mul2(num[q], inv));
     }
     st_words<NW>(out + (int64_t)f.r * a.head_dim + f.j, o);
@@ -360,7 +360,7 @@ __device__ __forceinline__ void bwd_compute(const SmallArgs &a, const BwdRow<RAT
 #pragma unroll
     for (int q = 0; q < NW; ++q) {
         g[q] = bf16x2_to_f2(f.g[q]);
-        inv[q] = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
+        inv[q] = make_float2(recip_den(den[q].x), recip_den(den[q].y));
         const float2 go = mul2(g[q], mul2(num[q], inv[q]));
         ngo[q] = make_float2(-go.x, -go.y);
     }

@@ -42,13 +42,78 @@ namespace cg = cooperative_groups;
 #define CSA_STREAM_BWD_CLUSTER 2
 #endif
 // Blocks per SM the forward's registers are capped for (1: no cap).
-#ifndef CSA_STREAM_FWD_MINB
-#define CSA_STREAM_FWD_MINB 1
+// Register cap of the forward: at 128 registers five-warp blocks fit three to an
+// SM (each SM sub-partition holds four such warps).
+#ifndef CSA_STREAM_FWD_MAXREG
+#define CSA_STREAM_FWD_MAXREG 128
+#endif
+#ifdef CSA_STREAM_BWD_MAXREG
+#define CSA_STREAM_BWD_BOUNDS __maxnreg__(CSA_STREAM_BWD_MAXREG)
+#else
+#define CSA_STREAM_BWD_BOUNDS __launch_bounds__(kMaxThreads)
+#endif
+
+#ifndef CSA_STREAM_PAIRS
+#define CSA_STREAM_PAIRS 2
 #endif
 
 namespace csa {
 
 namespace {
+
+constexpr int kNP = CSA_STREAM_PAIRS;  // fp32 column pairs per consumer thread
+constexpr int kCPT = 2 * kNP;          // columns per consumer thread
+constexpr int kColsPerWarp = 32 * kCPT;
+static_assert(kNP == 1 || kNP == 2, "CSA_STREAM_PAIRS is 1 or 2");
+constexpr int kMaxThreads = (512 / kColsPerWarp + 1) * 32;  // 512-column tile + the producer warp
+
+// kNP 32-bit words (2*kNP bf16): one 4- or 8-byte access.
+__device__ __forceinline__ void ld_np(uint32_t (&w)[kNP], const void *p)
+{
+    if constexpr (kNP == 2) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(p);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+        w[0] = *reinterpret_cast<const uint32_t *>(p);
+    }
+}
+
+__device__ __forceinline__ void st_np(void *p, const uint32_t (&w)[kNP])
+{
+    if constexpr (kNP == 2)
+        *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+    else
+        *reinterpret_cast<uint32_t *>(p) = w[0];
+}
+
+__device__ __forceinline__ void st_np_zero(void *p)
+{
+    if constexpr (kNP == 2)
+        *reinterpret_cast<uint2 *>(p) = make_uint2(0u, 0u);
+    else
+        *reinterpret_cast<uint32_t *>(p) = 0u;
+}
+
+// kNP fp32 pairs: one 8- or 16-byte access.
+__device__ __forceinline__ void ld_pairs(float2 (&v)[kNP], const float *p)
+{
+    if constexpr (kNP == 2) {
+        const float4 f = __ldg(reinterpret_cast<const float4 *>(p));
+        v[0] = make_float2(f.x, f.y);
+        v[1] = make_float2(f.z, f.w);
+    } else {
+        v[0] = __ldg(reinterpret_cast<const float2 *>(p));
+    }
+}
+
+__device__ __forceinline__ void st_pairs(float *p, const float2 (&v)[kNP])
+{
+    if constexpr (kNP == 2)
+        *reinterpret_cast<float4 *>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+    else
+        *reinterpret_cast<float2 *>(p) = v[0];
+}
 
 struct StreamArgs {
     const uint16_t *kv;
@@ -174,7 +239,7 @@ __device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int 
 
 template <int RATIO, int COFF>
 struct ApeRegs {
-    float2 v[COFF * RATIO][2];
+    float2 v[COFF * RATIO][kNP];
 };
 
 template <int RATIO, int COFF>
@@ -184,44 +249,46 @@ __device__ __forceinline__ void load_ape(const StreamArgs &a, int col0, ApeRegs<
 #pragma unroll
     for (int k = 0; k < COFF * RATIO; ++k) {
         const int p = k / RATIO, i = k % RATIO;
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(a.ape + i * C + (int64_t)p * a.head_dim + col0));
-        ap.v[k][0] = make_float2(v.x, v.y);
-        ap.v[k][1] = make_float2(v.z, v.w);
+        ld_pairs(ap.v[k], a.ape + i * C + (int64_t)p * a.head_dim + col0);
     }
 }
 
-// Reads the thread's two words (4 bf16) of window position k from the stage.
+// Reads the thread's kNP words (2*kNP bf16) of window position k from the stage.
 template <int RATIO, int COFF>
-__device__ __forceinline__ uint2 stage_words(const unsigned char *stage, int arr, int k, int tc, int lc)
+__device__ __forceinline__ void stage_words(uint32_t (&w)[kNP], const unsigned char *stage, int arr, int k, int tc,
+                                            int lc)
 {
     const int p = k / RATIO, i = k % RATIO;
-    return *reinterpret_cast<const uint2 *>(stage + stage_offset<RATIO, COFF>(arr, p, i, tc) + lc * 2);
+    ld_np(w, stage + stage_offset<RATIO, COFF>(arr, p, i, tc) + lc * 2);
 }
 
 template <int RATIO, int COFF>
 __device__ __forceinline__ void pool_stage(const unsigned char *stage, int tc, int lc, bool first,
-                                           const ApeRegs<RATIO, COFF> &ap, uint2 (&kvw)[COFF * RATIO],
-                                           float2 (&e)[COFF * RATIO][2], float2 (&den)[2], float2 (&num)[2])
+                                           const ApeRegs<RATIO, COFF> &ap, uint32_t (&kvw)[COFF * RATIO][kNP],
+                                           float2 (&e)[COFF * RATIO][kNP], float2 (&den)[kNP], float2 (&num)[kNP])
 {
     constexpr int W = COFF * RATIO;
-    float2 m[2] = {make_float2(-INFINITY, -INFINITY), make_float2(-INFINITY, -INFINITY)};
+    float2 m[kNP];
+#pragma unroll
+    for (int q = 0; q < kNP; ++q)
+        m[q] = make_float2(-INFINITY, -INFINITY);
 #pragma unroll
     for (int k = 0; k < W; ++k) {
         if (COFF == 2 && k < RATIO && first)
             continue;
-        const uint2 sw = stage_words<RATIO, COFF>(stage, 1, k, tc, lc);
-        kvw[k] = stage_words<RATIO, COFF>(stage, 0, k, tc, lc);
-        e[k][0] = add2(bf16x2_to_f2(sw.x), ap.v[k][0]);
-        e[k][1] = add2(bf16x2_to_f2(sw.y), ap.v[k][1]);
+        uint32_t sw[kNP];
+        stage_words<RATIO, COFF>(sw, stage, 1, k, tc, lc);
+        stage_words<RATIO, COFF>(kvw[k], stage, 0, k, tc, lc);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kNP; ++q) {
+            e[k][q] = add2(bf16x2_to_f2(sw[q]), ap.v[k][q]);
             m[q].x = max_nan(m[q].x, e[k][q].x);
             m[q].y = max_nan(m[q].y, e[k][q].y);
         }
     }
-    float2 negm[2];
+    float2 negm[kNP];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < kNP; ++q) {
         negm[q] = make_float2(-m[q].x, -m[q].y);
         den[q] = make_float2(0.0f, 0.0f);
         num[q] = make_float2(0.0f, 0.0f);
@@ -230,13 +297,12 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int tc, i
     for (int k = 0; k < W; ++k) {
         if (COFF == 2 && k < RATIO && first)
             continue;
-        const uint32_t kw[2] = {kvw[k].x, kvw[k].y};
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
+        for (int q = 0; q < kNP; ++q) {
             const float2 ek = exp2lanes(add2(e[k][q], negm[q]));
             e[k][q] = ek;
             den[q] = add2(den[q], ek);
-            num[q] = fma2(ek, bf16x2_to_f2(kw[q]), num[q]);
+            num[q] = fma2(ek, bf16x2_to_f2(kvw[k][q]), num[q]);
         }
     }
 }
@@ -244,11 +310,11 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int tc, i
 // ----------------------------------------------------------------- forward
 
 template <int RATIO, int COFF>
-__global__ void __launch_bounds__(160, CSA_STREAM_FWD_MINB) fwd_stream_kernel(StreamArgs a, uint16_t *__restrict__ out)
+__global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG) fwd_stream_kernel(StreamArgs a, uint16_t *__restrict__ out)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int ncw = blockDim.x / 32 - 1;  // consumer warps; the last warp produces
-    const int tc = ncw * 128;
+    const int tc = ncw * kColsPerWarp;
     const int c0 = blockIdx.y * tc;
     const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -265,7 +331,7 @@ __global__ void __launch_bounds__(160, CSA_STREAM_FWD_MINB) fwd_stream_kernel(St
             produce<RATIO, COFF, false>(a, s, tc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
         return;
     }
-    const int lc = threadIdx.x * 4;  // local column of this thread in the tile
+    const int lc = threadIdx.x * kCPT;  // local column of this thread in the tile
     ApeRegs<RATIO, COFF> ap;
     load_ape<RATIO, COFF>(a, c0 + lc, ap);
     int st = 0;
@@ -275,17 +341,17 @@ __global__ void __launch_bounds__(160, CSA_STREAM_FWD_MINB) fwd_stream_kernel(St
             break;
         const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
         const bool first = s.meta[st].first;
-        uint2 kvw[COFF * RATIO];
-        float2 e[COFF * RATIO][2], den[2], num[2];
+        uint32_t kvw[COFF * RATIO][kNP];
+        float2 e[COFF * RATIO][kNP], den[kNP], num[kNP];
         pool_stage<RATIO, COFF>(stage, tc, lc, first, ap, kvw, e, den, num);
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
-        uint32_t o[2];
+        uint32_t o[kNP];
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
-            o[q] = f2_to_bf16x2(mul2(num[q], make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y))));
-        *reinterpret_cast<uint2 *>(out + (int64_t)row * a.head_dim + c0 + lc) = make_uint2(o[0], o[1]);
+        for (int q = 0; q < kNP; ++q)
+            o[q] = f2_to_bf16x2(mul2(num[q], make_float2(recip_den(den[q].x), recip_den(den[q].y))));
+        st_np(out + (int64_t)row * a.head_dim + c0 + lc, o);
         if (++st == a.stages) {
             st = 0;
             ph ^= 1u;
@@ -309,8 +375,8 @@ __device__ __forceinline__ void zero_range(const GradOut &o, int64_t C, int head
     for (int64_t t = t0 < 0 ? 0 : t0; t < t1; ++t) {
 #pragma unroll
         for (int p = 0; p < COFF; ++p) {
-            *reinterpret_cast<uint2 *>(o.dkv + t * C + p * head_dim + col) = make_uint2(0u, 0u);
-            *reinterpret_cast<uint2 *>(o.dscore + t * C + p * head_dim + col) = make_uint2(0u, 0u);
+            st_np_zero(o.dkv + t * C + p * head_dim + col);
+            st_np_zero(o.dscore + t * C + p * head_dim + col);
         }
     }
 }
@@ -322,7 +388,7 @@ __device__ __forceinline__ void zero_range(const GradOut &o, int64_t C, int head
 // is merged across the cluster in ascending rank order through distributed shared
 // memory; dape_finalize_kernel sums the cluster partials in a fixed order.
 template <int RATIO, int COFF>
-__global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n_tokens_arg,
+__global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_tokens_arg,
                                                          const uint16_t *__restrict__ grad_out,
                                                          uint16_t *__restrict__ dkv, uint16_t *__restrict__ dscore,
                                                          float *__restrict__ partial)
@@ -330,7 +396,7 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
     constexpr int W = COFF * RATIO;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int ncw = blockDim.x / 32 - 1;
-    const int tc = ncw * 128;
+    const int tc = ncw * kColsPerWarp;
     const int c0 = blockIdx.y * tc;
     const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -350,11 +416,13 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
     }
     __syncthreads();
 
-    float2 acc[W][2];
+    float2 acc[W][kNP];
 #pragma unroll
     for (int k = 0; k < W; ++k)
-        acc[k][0] = acc[k][1] = make_float2(0.0f, 0.0f);
-    const int lc = threadIdx.x * 4;
+#pragma unroll
+        for (int q = 0; q < kNP; ++q)
+            acc[k][q] = make_float2(0.0f, 0.0f);
+    const int lc = threadIdx.x * kCPT;
     const int col = c0 + lc;
 
     if (warp == ncw) {
@@ -387,18 +455,19 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
                 continue;
             }
             const unsigned char *stage = s.stages + (size_t)st_used * a.stage_bytes;
-            uint2 kvw[W];
-            float2 e[W][2], den[2], num[2];
+            uint32_t kvw[W][kNP];
+            float2 e[W][kNP], den[kNP], num[kNP];
             pool_stage<RATIO, COFF>(stage, tc, lc, m.first, ap, kvw, e, den, num);
-            const uint2 gw = *reinterpret_cast<const uint2 *>(stage + window_bytes<RATIO, COFF>(tc) + lc * 2);
+            uint32_t gw[kNP];
+            ld_np(gw, stage + window_bytes<RATIO, COFF>(tc) + lc * 2);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&s.empty[st_used]));
-            const float2 g[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
-            float2 inv[2], ngo[2];
+            float2 g[kNP], inv[kNP], ngo[kNP];
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                inv[q] = make_float2(__frcp_rn(den[q].x), __frcp_rn(den[q].y));
+            for (int q = 0; q < kNP; ++q) {
+                g[q] = bf16x2_to_f2(gw[q]);
+                inv[q] = make_float2(recip_den(den[q].x), recip_den(den[q].y));
                 const float2 go = mul2(g[q], mul2(num[q], inv[q]));
                 ngo[q] = make_float2(-go.x, -go.y);
             }
@@ -408,20 +477,19 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
                     continue;
                 const int p = k / RATIO, i = k % RATIO;
                 const int64_t tok = m.base + (int64_t)(p - (COFF - 1)) * RATIO + i;
-                const uint32_t kw[2] = {kvw[k].x, kvw[k].y};
-                uint32_t dk[2], dsw[2];
+                uint32_t dk[kNP], dsw[kNP];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
+                for (int q = 0; q < kNP; ++q) {
                     const float2 pk = mul2(e[k][q], inv[q]);
                     dk[q] = f2_to_bf16x2(mul2(g[q], pk));
-                    const float2 ds = mul2(pk, add2(mul2(g[q], bf16x2_to_f2(kw[q])), ngo[q]));
+                    const float2 ds = mul2(pk, add2(mul2(g[q], bf16x2_to_f2(kvw[k][q])), ngo[q]));
                     dsw[q] = f2_to_bf16x2(ds);
                     acc[k][q] = add2(acc[k][q], ds);
                 }
                 if (tok < o.n_tokens) {
                     const int64_t gi = tok * C + (int64_t)p * a.head_dim + col;
-                    *reinterpret_cast<uint2 *>(dkv + gi) = make_uint2(dk[0], dk[1]);
-                    *reinterpret_cast<uint2 *>(dscore + gi) = make_uint2(dsw[0], dsw[1]);
+                    st_np(dkv + gi, dk);
+                    st_np(dscore + gi, dsw);
                 }
             }
             if (m.row + 1 == __ldg(a.cc + m.seg + 1)) {  // last block of its segment
@@ -429,8 +497,8 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
                     for (int i = 0; i < RATIO; ++i) {
                         const int64_t tok = m.base + i;
                         if (tok < o.n_tokens) {
-                            *reinterpret_cast<uint2 *>(dkv + tok * C + col) = make_uint2(0u, 0u);
-                            *reinterpret_cast<uint2 *>(dscore + tok * C + col) = make_uint2(0u, 0u);
+                            st_np_zero(dkv + tok * C + col);
+                            st_np_zero(dscore + tok * C + col);
                         }
                     }
                 }
@@ -444,8 +512,7 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
 #pragma unroll
         for (int k = 0; k < W; ++k) {
             const int p = k / RATIO, i = k % RATIO;
-            float *sp = s.red + (i * COFF + p) * tc + lc;
-            *reinterpret_cast<float4 *>(sp) = make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
+            st_pairs(s.red + (i * COFF + p) * tc + lc, acc[k]);
         }
     }
     __syncthreads();
@@ -475,11 +542,12 @@ __global__ void __launch_bounds__(160) bwd_stream_kernel(StreamArgs a, int64_t n
     cluster.sync();
 }
 
+// Widest tile of at most 512 columns (whole consumer warps) that divides head_dim.
 int tile_cols(int head_dim)
 {
-    for (int tc : {512, 384, 256, 128})
-        if (head_dim % tc == 0)
-            return tc;
+    for (int w = 512 / kColsPerWarp; w >= 1; --w)
+        if (head_dim % (w * kColsPerWarp) == 0)
+            return w * kColsPerWarp;
     return 0;
 }
 
@@ -495,7 +563,7 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     StreamPlan pl;
     pl.tc = tile_cols(head_dim);
     pl.tiles = head_dim / pl.tc;
-    pl.threads = (pl.tc / 128 + 1) * 32;
+    pl.threads = (pl.tc / kColsPerWarp + 1) * 32;
     const int win = 2 * coff * ratio * pl.tc * 2;
     pl.stage_bytes = ((bwd ? win + pl.tc * 2 : win) + 127) / 128 * 128;
     const int budget = bwd ? CSA_STREAM_BWD_BUDGET : CSA_STREAM_FWD_BUDGET;
