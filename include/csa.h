@@ -130,12 +130,12 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * could block, a plug-in that may not use the CUDA allocator.
  *
  * Same arguments, results and errors as csa_compress_bwd (bitwise the same
- * outputs), except that the grad_ape partial sums go to a fixed 4 MiB array in
+ * outputs), except that the grad_ape partial sums go to a fixed 6 MiB array in
  * the library's device code instead of the library's memory pool.  That array
- * occupies 4 MiB on every GPU that loads the library, until the process exits.
+ * occupies 6 MiB on every GPU that loads the library, until the process exits.
  * A shape that needs more partial storage than the array holds is rejected with
- * CSA_ERR_TOO_LARGE before anything is launched (on a 152-SM GB300 every ratio-4
- * shape fits, and ratio-128 shapes up to coff * head_dim = 1024).  No cudaMalloc,
+ * CSA_ERR_TOO_LARGE before anything is launched (on a 152-SM GB300 every shape
+ * fits except ratio 128 with coff 2 and head_dim above 6144).  No cudaMalloc,
  * cudaFree or other allocating call is made.
  *
  * Every call on a device shares the array and leaves its contents behind; each
@@ -191,7 +191,7 @@ CSA_API int csa_selftest_bounded_wait(int64_t limit_ns, void *stream);
  * Self-test of the reciprocal the kernels take of each softmax denominator (the
  * pages have no counterpart: they only fix fp32 arithmetic).  Writes, for i < n,
  * out[i] = the library's 1/d[i]; that routine is correctly rounded for d in
- * [1, 256], the range every denominator falls in (NaN in, NaN out), and is
+ * [2^-8, 2^8], which holds every denominator (NaN in, NaN out), and is
  * unspecified elsewhere.  d and out are device pointers to n floats, 4-byte
  * aligned, not overlapping; n >= 0 (n == 0 launches nothing).  Asynchronous on
  * `stream`.  Returns CSA_ERR_INVALID_VALUE for a NULL pointer with n > 0 or for

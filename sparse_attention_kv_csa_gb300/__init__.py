@@ -147,7 +147,7 @@ def csa_compress_bwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, 
 def csa_compress_bwd_noalloc(kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                              capacity, n_tokens, grad_out, dkv, dscore, dape, stream=None) -> None:
     """csa_compress_bwd for callers that cannot allocate: its scratch is a fixed
-    4 MiB array of the library (shared by all calls on a device; see csa.h)."""
+    6 MiB array of the library (shared by all calls on a device; see csa.h)."""
     _check(_lib.csa_compress_bwd_noalloc(_addr(kv), _addr(score), _addr(ape), _addr(cu_seqlens),
                                          _addr(cu_seqlens_comp), n_seg, ratio, coff, head_dim, capacity,
                                          n_tokens, _addr(grad_out), _addr(dkv), _addr(dscore), _addr(dape),

@@ -33,8 +33,9 @@ __device__ __forceinline__ float max_nan(float a, float b)
 }
 
 // ----------------------------------------------------------- reciprocal
-// 1/d rounded to nearest for d in [1, 256]: the range of a softmax denominator
-// whose largest term is exactly 1 and which has at most 256 terms (NaN stays NaN).
+// 1/d rounded to nearest for d in [2^-8, 2^8], which holds every softmax
+// denominator here: at most 256 terms, the largest 1 or within a few ulp of it
+// (NaN stays NaN).
 // Seed: the hardware approximation rcp.approx, within one ulp of 1/d by the PTX
 // ISA.  One Newton-Raphson correction in Markstein's fused form (P. Markstein,
 // IBM J. Res. Dev. 34(1), 1990): the residual r = 1 - d*y is exact in one FMA, and
@@ -43,7 +44,8 @@ __device__ __forceinline__ float max_nan(float a, float b)
 // lies just above a rounding tie, the seed 2^(-k-1) lands on the tie, and the
 // correctly rounded result 2^(-k-1) (1 + 2^-23) is the step's result with its
 // lowest bit set.  Both statements hold exhaustively over one binade, and the step
-// commutes with scaling by a power of two on this range.
+// commutes with scaling by a power of two on this range (no intermediate leaves
+// the normal range).
 __device__ __forceinline__ float recip_den(float d)
 {
     float y;

@@ -6,7 +6,7 @@
 // step, a real-time loop in which growing or trimming a pool could block, or a
 // plug-in that is not allowed to touch the CUDA allocator at all.  This entry
 // point runs the same kernels with the scratch in a fixed array of this file
-// (kScratchFloats floats, 4 MiB) that lives in every GPU's memory from the moment
+// (kScratchFloats floats, 6 MiB) that lives in every GPU's memory from the moment
 // the library's device code is loaded until the process exits.  It calls no
 // cudaMalloc / cudaFree or allocating routine.
 //
@@ -23,10 +23,10 @@
 #include "csa.h"
 #include "csa_launch.h"
 
-// Scratch for the grad_ape partials: 1048576 floats = 4 MiB per GPU.  Every
-// ratio-4 shape and the ratio-128 shapes with coff * head_dim up to 1024 fit on a
-// 152-SM GB300; wider ratio-128 shapes are rejected.
-static constexpr size_t kScratchFloats = 1024u * 1024u;
+// Scratch for the grad_ape partials: 1572864 floats = 6 MiB per GPU.  On a
+// 152-SM GB300 every shape fits except ratio 128 with coff 2 and head_dim above
+// 6144, which is rejected.
+static constexpr size_t kScratchFloats = 1536u * 1024u;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 // Status word of the bounded waits of calls made through this entry point.
 static __device__ __align__(256) unsigned g_noalloc_status[64];

@@ -15,11 +15,15 @@
 //
 // Order of the arithmetic (the page's ratio-128 family: a deterministic chunked
 // order, checked against the plain sequential oracle by tolerance):
-//   s_k = score + ape;  m = max over all valid k (exact: chunk maxima, then the
-//   maximum of those);  e_k = exp(s_k - m) (the library's exp);
+//   s_k = score + ape;  m = max over all valid k (exact: chunk maxima, then over
+//   the warp's chunks by shuffles, then over the eight warps);
+//   e_k = 2^(s_k*log2(e) - m*log2(e)) on the multi-function unit (ex2.approx, as
+//   the page's ratio-128 kernels do: ~2^-22 relative error, far below the final
+//   bf16 rounding);
 //   den_c = ((+0 + e_c) + e_c+NC) + ... within chunk c, num_c = fma chain;
-//   den = ((+0 + den_0) + den_1) + ... over chunks ascending, num likewise;
-//   inv = rcp.rn(den);  o = num * inv;  out = bf16(o).
+//   chunk sums added over the warp's chunks by a fixed xor-shuffle tree, warp sums
+//   added in ascending warp pairs and then by a fixed xor-shuffle tree over the
+//   threads of a column;  inv = 1/den rounded;  o = num * inv;  out = bf16(o).
 // Backward per valid k: p = e_k * inv;  grad_kv = bf16(g*p);
 //   ds = p*(g*kv - g*o);  grad_score = bf16(ds); grad_ape as in the other kernels
 //   (per-thread sums over its rows, cluster merge in rank order, fixed-order
@@ -39,7 +43,7 @@
 namespace cg = cooperative_groups;
 
 #ifndef CSA_R128_BWD_CLUSTER
-#define CSA_R128_BWD_CLUSTER 4
+#define CSA_R128_BWD_CLUSTER 1
 #endif
 
 namespace csa {
@@ -59,6 +63,7 @@ struct Geo {
     static constexpr int CW = NC / CPW;       // consumer warps (8)
     static constexpr int CT = CW * 32;        // consumer threads
     static constexpr int THREADS = CT + 32;   // + one producer warp
+    static constexpr int RS = TC + 4;         // row stride of the merge buffers
     static constexpr int BOX_BYTES = kR * TC * 2;
     static constexpr int WIN_BYTES = 2 * COFF * BOX_BYTES;
 };
@@ -89,9 +94,9 @@ struct Meta {
 template <int COFF>
 struct R128Smem {
     unsigned char *stages;
-    float *mx;   // [2][NC][TC]
-    float *den;  // [2][NC][TC]
-    float *num;  // [2][NC][TC]
+    float *mx;   // [2][CW][RS]  warp maxima
+    float *den;  // [2][CW][RS]  warp sums
+    float *num;  // [2][CW][RS]
     float *fin;  // [2][2][TC]  (inv, g*o) for the backward
     Meta *meta;
     uint64_t *full;
@@ -102,7 +107,7 @@ template <int COFF>
 __host__ __device__ size_t r128_smem_bytes(int stages, int stage_bytes)
 {
     using G = Geo<COFF>;
-    return (size_t)stages * stage_bytes + 3 * 2 * G::NC * G::TC * 4 + 2 * 2 * G::TC * 4 + sizeof(Meta) * stages +
+    return (size_t)stages * stage_bytes + 3 * 2 * G::CW * G::RS * 4 + 2 * 2 * G::TC * 4 + sizeof(Meta) * stages +
            16 * stages + 16;
 }
 
@@ -114,9 +119,9 @@ __device__ __forceinline__ R128Smem<COFF> r128_carve(unsigned char *base, int st
     s.stages = base;
     unsigned char *p = base + (size_t)stages * stage_bytes;
     s.mx = reinterpret_cast<float *>(p);
-    s.den = s.mx + 2 * G::NC * G::TC;
-    s.num = s.den + 2 * G::NC * G::TC;
-    s.fin = s.num + 2 * G::NC * G::TC;
+    s.den = s.mx + 2 * G::CW * G::RS;
+    s.num = s.den + 2 * G::CW * G::RS;
+    s.fin = s.num + 2 * G::CW * G::RS;
     p = reinterpret_cast<unsigned char *>(s.fin + 2 * 2 * G::TC);
     s.meta = reinterpret_cast<Meta *>(p);
     s.full = reinterpret_cast<uint64_t *>(s.meta + stages);
@@ -237,37 +242,55 @@ __device__ __forceinline__ void r128_load(const unsigned char *stage, int c, int
     }
 }
 
+constexpr float kLog2eF = 1.4426950408889634f;
+
+// 2^x on the multi-function unit (flushes results below 2^-126 to zero).
+__device__ __forceinline__ float ex2_fast(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // The two merge phases of one row.  Every consumer thread calls this once per
 // row.  The first barrier also votes on `ok` (the thread's wait for the row's
 // data succeeded): if any thread failed, all return false together before the
 // second barrier.  `have`: the row has data (cs loaded).  On true: cs.e holds e_k
-// of the thread's valid positions, and the chunk sums are in the merge buffers
-// for r128_merge.
+// of the thread's valid positions, and each warp's sums over its chunks are in
+// the merge buffers for r128_final.
 template <int COFF>
 __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int c, int g, bool ok, bool have,
                                           bool first, ChunkState &cs)
 {
     using G = Geo<COFF>;
-    float2 m = make_float2(-INFINITY, -INFINITY), m2 = m;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (have) {
 #pragma unroll
         for (int i = 0; i < kKC; ++i) {
             if (!pos_valid<COFF>(c, i, first))
                 continue;
-            m.x = max_nan(m.x, cs.e[i][0].x);
-            m.y = max_nan(m.y, cs.e[i][0].y);
-            m2.x = max_nan(m2.x, cs.e[i][1].x);
-            m2.y = max_nan(m2.y, cs.e[i][1].y);
+            m[0] = max_nan(m[0], cs.e[i][0].x);
+            m[1] = max_nan(m[1], cs.e[i][0].y);
+            m[2] = max_nan(m[2], cs.e[i][1].x);
+            m[3] = max_nan(m[3], cs.e[i][1].y);
         }
     }
-    float *mx = s.mx + (size_t)buf * G::NC * G::TC;
-    *reinterpret_cast<float4 *>(mx + c * G::TC + 4 * g) = make_float4(m.x, m.y, m2.x, m2.y);
+    // over the warp's chunks: lanes g, g + G, g + 2G, ... hold the same columns
+#pragma unroll
+    for (int d = G::G; d < 32; d *= 2)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            m[q] = max_nan(m[q], __shfl_xor_sync(0xffffffffu, m[q], d));
+    float *mx = s.mx + (size_t)buf * G::CW * G::RS;
+    if (lane < G::G)
+        *reinterpret_cast<float4 *>(mx + warp * G::RS + 4 * g) = make_float4(m[0], m[1], m[2], m[3]);
     if (!named_barrier_and(1, G::CT, ok))
         return false;
     float4 M = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-#pragma unroll 8
-    for (int cc = 0; cc < G::NC; ++cc) {
-        const float4 v = *reinterpret_cast<const float4 *>(mx + cc * G::TC + 4 * g);
+#pragma unroll
+    for (int w = 0; w < G::CW; ++w) {
+        const float4 v = *reinterpret_cast<const float4 *>(mx + w * G::RS + 4 * g);
         M.x = max_nan(M.x, v.x);
         M.y = max_nan(M.y, v.y);
         M.z = max_nan(M.z, v.z);
@@ -275,7 +298,9 @@ __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int 
     }
     float2 den[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
     float2 num[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-    const float2 negm[2] = {make_float2(-M.x, -M.y), make_float2(-M.z, -M.w)};
+    // exponent s*log2(e) - m*log2(e): one fma per element
+    const float2 nml[2] = {make_float2(-__fmul_rn(M.x, kLog2eF), -__fmul_rn(M.y, kLog2eF)),
+                           make_float2(-__fmul_rn(M.z, kLog2eF), -__fmul_rn(M.w, kLog2eF))};
 #pragma unroll
     for (int i = 0; i < kKC; ++i) {
         if (!have || !pos_valid<COFF>(c, i, first))
@@ -283,33 +308,60 @@ __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int 
         const uint32_t kw[2] = {cs.kv[i].x, cs.kv[i].y};
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const float2 ek = exp2lanes(add2(cs.e[i][q], negm[q]));
+            const float2 x = fma2(cs.e[i][q], splat(kLog2eF), nml[q]);
+            const float2 ek = make_float2(ex2_fast(x.x), ex2_fast(x.y));
             cs.e[i][q] = ek;
             den[q] = add2(den[q], ek);
             num[q] = fma2(ek, bf16x2_to_f2(kw[q]), num[q]);
         }
     }
-    float *dn = s.den + (size_t)buf * G::NC * G::TC;
-    float *nm = s.num + (size_t)buf * G::NC * G::TC;
-    *reinterpret_cast<float4 *>(dn + c * G::TC + 4 * g) = make_float4(den[0].x, den[0].y, den[1].x, den[1].y);
-    *reinterpret_cast<float4 *>(nm + c * G::TC + 4 * g) = make_float4(num[0].x, num[0].y, num[1].x, num[1].y);
+    // over the warp's chunks, a fixed xor tree (both partners add the same two
+    // values: the sums agree bitwise)
+#pragma unroll
+    for (int d = G::G; d < 32; d *= 2)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            den[q] = add2(den[q], make_float2(__shfl_xor_sync(0xffffffffu, den[q].x, d),
+                                              __shfl_xor_sync(0xffffffffu, den[q].y, d)));
+            num[q] = add2(num[q], make_float2(__shfl_xor_sync(0xffffffffu, num[q].x, d),
+                                              __shfl_xor_sync(0xffffffffu, num[q].y, d)));
+        }
+    if (lane < G::G) {
+        float *dn = s.den + (size_t)buf * G::CW * G::RS;
+        float *nm = s.num + (size_t)buf * G::CW * G::RS;
+        *reinterpret_cast<float4 *>(dn + warp * G::RS + 4 * g) = make_float4(den[0].x, den[0].y, den[1].x, den[1].y);
+        *reinterpret_cast<float4 *>(nm + warp * G::RS + 4 * g) = make_float4(num[0].x, num[0].y, num[1].x, num[1].y);
+    }
     named_barrier(1, G::CT);
     return true;
 }
 
-// The fixed-order chunk merge of tile column j: den and num.
+// The fixed-order merge of the eight warp sums, spread over all consumer threads:
+// TPC consecutive threads own tile column j; each adds its warps' sums in
+// ascending order, then the TPC partial sums meet in a fixed xor-shuffle tree, so
+// every one of them ends with the same den and num of column j.
 template <int COFF>
-__device__ __forceinline__ void r128_merge(const R128Smem<COFF> &s, int buf, int j, float &den, float &num)
+__device__ __forceinline__ void r128_final(const R128Smem<COFF> &s, int buf, int &j, float &den, float &num)
 {
     using G = Geo<COFF>;
-    const float *dn = s.den + (size_t)buf * G::NC * G::TC;
-    const float *nm = s.num + (size_t)buf * G::NC * G::TC;
-    den = 0.0f;
-    num = 0.0f;
-#pragma unroll 8
-    for (int cc = 0; cc < G::NC; ++cc) {
-        den = __fadd_rn(den, dn[cc * G::TC + j]);
-        num = __fadd_rn(num, nm[cc * G::TC + j]);
+    constexpr int TPC = G::CT / G::TC;  // threads per column
+    constexpr int WPT = G::CW / TPC;    // warp sums per thread
+    static_assert(TPC * G::TC == G::CT && WPT * TPC == G::CW, "merge split");
+    j = (int)threadIdx.x / TPC;
+    const int q = (int)threadIdx.x % TPC;
+    const float *dn = s.den + (size_t)buf * G::CW * G::RS + q * WPT * G::RS + j;
+    const float *nm = s.num + (size_t)buf * G::CW * G::RS + q * WPT * G::RS + j;
+    den = dn[0];
+    num = nm[0];
+#pragma unroll
+    for (int w = 1; w < WPT; ++w) {
+        den = __fadd_rn(den, dn[w * G::RS]);
+        num = __fadd_rn(num, nm[w * G::RS]);
+    }
+#pragma unroll
+    for (int d = 1; d < TPC; d *= 2) {
+        den = __fadd_rn(den, __shfl_xor_sync(0xffffffffu, den, d));
+        num = __fadd_rn(num, __shfl_xor_sync(0xffffffffu, num, d));
     }
 }
 
@@ -369,12 +421,14 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
         }
         if (!r128_pool<COFF>(s, buf, c, g, ok, ok, first, cs))
             break;
-        if (c < 4) {
-            const int j = 4 * g + c;
+        {
+            int j;
             float den, num;
-            r128_merge<COFF>(s, buf, j, den, num);
-            const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, recip_den(den)));
-            out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
+            r128_final<COFF>(s, buf, j, den, num);
+            if (threadIdx.x % (G::CT / G::TC) == 0) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, recip_den(den)));
+                out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
+            }
         }
         buf ^= 1;
     }
@@ -469,23 +523,25 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
                 break;
             const float2 gg[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
             float *fin = s.fin + (size_t)buf * 2 * G::TC;
-            if (c < 4) {
-                const int j = 4 * g + c;
+            {
+                int j;
                 float den, num;
-                r128_merge<COFF>(s, buf, j, den, num);
-                const float inv = recip_den(den);
-                const float gj = c == 0 ? gg[0].x : c == 1 ? gg[0].y : c == 2 ? gg[1].x : gg[1].y;
-                fin[j] = inv;
-                fin[G::TC + j] = __fmul_rn(gj, __fmul_rn(num, inv));
+                r128_final<COFF>(s, buf, j, den, num);
+                if (threadIdx.x % (G::CT / G::TC) == 0 && m.real) {
+                    const float inv = recip_den(den);
+                    fin[j] = inv;
+                    fin[G::TC + j] = __fmul_rn(num, inv);  // o
+                }
             }
             named_barrier(1, G::CT);
             buf ^= 1;
             if (!m.real)
                 continue;
             const float4 inv4 = *reinterpret_cast<const float4 *>(fin + 4 * g);
-            const float4 go4 = *reinterpret_cast<const float4 *>(fin + G::TC + 4 * g);
+            const float4 o4 = *reinterpret_cast<const float4 *>(fin + G::TC + 4 * g);
             const float2 inv[2] = {make_float2(inv4.x, inv4.y), make_float2(inv4.z, inv4.w)};
-            const float2 ngo[2] = {make_float2(-go4.x, -go4.y), make_float2(-go4.z, -go4.w)};
+            const float2 go[2] = {mul2(gg[0], make_float2(o4.x, o4.y)), mul2(gg[1], make_float2(o4.z, o4.w))};
+            const float2 ngo[2] = {make_float2(-go[0].x, -go[0].y), make_float2(-go[1].x, -go[1].y)};
 #pragma unroll
             for (int i = 0; i < kKC; ++i) {
                 if (!pos_valid<COFF>(c, i, first))

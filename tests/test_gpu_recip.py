@@ -1,6 +1,6 @@
 """The kernels' softmax-denominator reciprocal on the GPU (through the C ABI's
 self-test hook) against numpy's IEEE round-to-nearest 1/d: every float in [1, 2),
-samples of every binade up to 256, the all-ones significands, and NaN."""
+samples of every binade from 2^-8 to 2^8, the all-ones significands, and NaN."""
 import numpy as np
 import pytest
 
@@ -28,11 +28,11 @@ def test_reciprocal_every_float_in_one_binade():
 def test_reciprocal_other_binades_and_edges():
     rng = np.random.default_rng(11)
     parts = []
-    for k in range(0, 8):
+    for k in range(-8, 8):
         m = rng.integers(0, 1 << 23, 1 << 20, dtype=np.uint32)
         parts.append((m | np.uint32((127 + k) << 23)).view(np.float32))
         parts.append(np.array([(np.uint32((127 + k) << 23) | np.uint32(0x7FFFFF))], dtype=np.uint32).view(np.float32))
-    parts.append(np.array([1.0, 2.0, 3.0, 7.0, 8.0, 255.99998, 256.0], dtype=np.float32))
+    parts.append(np.array([2.0 ** -8, 0.99999994, 1.0, 2.0, 3.0, 7.0, 8.0, 255.99998, 256.0], dtype=np.float32))
     d = np.concatenate(parts)
     got = _run(d)
     want = np.float32(1) / d

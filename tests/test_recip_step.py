@@ -1,11 +1,11 @@
-"""The kernels take the reciprocal of each softmax denominator d in [1, 256] (the
-largest term is exactly 1 and there are at most 256 terms) by one Newton-Raphson
+"""The kernels take the reciprocal of each softmax denominator d (at most 256
+terms, the largest 1 or within a few ulp of it: d in [2^-8, 2^8]) by one Newton-Raphson
 correction, in Markstein's fused form, of a hardware seed y within one ulp of 1/d:
 r = fma(-d, y, 1); y1 = fma(y, r, y); and when the significand of d is all ones the
 lowest bit of y1 is set.  The claim is that this equals the IEEE round-to-nearest
 1/d for EVERY seed within one ulp.  Here it is checked exhaustively over the binade
 [1, 2) with exact emulation of the two fused operations, and on samples of every
-other binade up to 256 (the step commutes with scaling by 2^k there).
+other binade from 2^-8 to 2^8 (the step commutes with scaling by 2^k there).
 
 The fused operations are emulated exactly: d*y has 48 significant bits and is
 exact in float64, so 1 - d*y (|r| < 2^-22) is exact too and rounding it to
@@ -69,7 +69,7 @@ def test_reciprocal_step_exhaustive_over_one_binade():
 
 def test_reciprocal_step_other_binades_sampled():
     rng = np.random.default_rng(7)
-    for k in range(1, 8):                           # [2, 4) ... [128, 256)
+    for k in list(range(-8, 0)) + list(range(1, 8)):  # [2^-8, 2^-7) ... [128, 256)
         m = rng.integers(0, 1 << 23, 200000, dtype=np.uint32)
         m[:3] = (0, 1, (1 << 23) - 1)
         d = (m | np.uint32((127 + k) << 23)).view(np.float32)

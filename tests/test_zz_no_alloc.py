@@ -77,7 +77,7 @@ def test_noalloc_ratio128_matches_backward(csa):
 
 def test_noalloc_rejects_shape_beyond_its_scratch(csa):
     """ratio 128, coff 2, head_dim 8192: one grad_ape partial is 128 x 16384 floats
-    (8 MiB), more than the fixed array holds: rejected before launch."""
+    (8 MiB), more than the fixed 6 MiB array holds: rejected before launch."""
     import torch
     c = w.make_case("na_big", 128, 2, 8192, [256], seed=6)
     d = Dev(c)
