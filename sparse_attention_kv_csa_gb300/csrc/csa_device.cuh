@@ -168,6 +168,16 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinte
 
 }  // namespace csa
 
+// ----------------------------------------- programmatic dependent launch
+// Every compute kernel of the library is launched so that its blocks may become
+// resident while the previous kernel in the stream is still finishing.  pdl_wait()
+// holds the grid until that kernel has completed and its memory operations are
+// visible (it returns at once after any other predecessor); a kernel reads and
+// writes no global memory before it.  pdl_trigger() then lets the next such
+// launch do the same.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------- async copies, barriers
 // Shared-memory mbarriers and raw bulk copies (cp.async.bulk: contiguous global
 // bytes -> shared memory, completion counted on an mbarrier in bytes).

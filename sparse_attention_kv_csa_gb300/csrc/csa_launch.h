@@ -7,6 +7,16 @@
 
 namespace csa {
 
+// Launch attribute that lets a kernel start while its stream predecessor finishes
+// (the kernel itself waits for it before touching memory: pdl_wait()).
+inline cudaLaunchAttribute pdl_attribute()
+{
+    cudaLaunchAttribute a = {};
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 struct FwdParams {
     const void *kv;
     const void *score;

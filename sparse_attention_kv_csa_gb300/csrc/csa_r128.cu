@@ -396,6 +396,8 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     r128_init<COFF>(s, a.stages);
+    pdl_wait();
+    pdl_trigger();
     if (warp == G::CW) {
         if (lane == 0)
             r128_produce<COFF, false>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
@@ -470,12 +472,13 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t C = (int64_t)COFF * a.head_dim;
+    r128_init<COFF>(s, a.stages);
+    pdl_wait();
+    pdl_trigger();  // the grad_ape finalisation may launch; it waits for this grid's end
     const int R = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;
     const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
     const int rend = R < a.capacity ? R : a.capacity;
     const int64_t n_tokens = n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg);
-    asm volatile("griddepcontrol.launch_dependents;");
-    r128_init<COFF>(s, a.stages);
 
     const int g = lane % G::G, c = G::CPW * warp + lane / G::G;
     const int col = c0 + 4 * g;  // thread's first column within a half
@@ -758,9 +761,15 @@ cudaError_t launch_fwd_r128_t(const FwdParams &p, unsigned *status, cudaStream_t
         return e;
     R128Args a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
                p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes, status};
-    fwd_r128_kernel<COFF><<<dim3(blocks, pl.tiles), pl.threads, pl.smem, st>>>(a, mk, ms,
-                                                                              static_cast<uint16_t *>(p.out));
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, pl.tiles, 1);
+    cfg.blockDim = dim3(pl.threads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fwd_r128_kernel<COFF>, a, mk, ms, static_cast<uint16_t *>(p.out));
 }
 
 template <int COFF>
@@ -787,13 +796,14 @@ cudaError_t launch_bwd_r128_t(const BwdParams &p, float *partial, int blocks, un
     cfg.blockDim = dim3(pl.threads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = pl.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, bwd_r128_kernel<COFF>, a, mk, ms, p.n_tokens,
                            static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
                            static_cast<uint16_t *>(p.dscore), partial);

@@ -265,6 +265,8 @@ __device__ __forceinline__ void fwd_compute(const SmallArgs &a, const FwdUnit<RA
 template <int RATIO, int COFF>
 __global__ void __launch_bounds__(kFwdThreads, CSA_FWD_MINB) fwd_small_kernel(SmallArgs a, uint16_t *__restrict__ out)
 {
+    pdl_wait();
+    pdl_trigger();
     const int groups = a.head_dim / (2 * kFwdNW);
     const int total = a.capacity * groups;
     const int stride = gridDim.x * blockDim.x;
@@ -432,8 +434,8 @@ __global__ void __launch_bounds__(kBwdThreads, CSA_BWD_MINB)
     constexpr int W = COFF * RATIO;
     constexpr int NW = kBwdNW;
     extern __shared__ float red[];
-    // Let the grad_ape finalisation grid launch now; it waits for this grid's end.
-    asm volatile("griddepcontrol.launch_dependents;");
+    pdl_wait();
+    pdl_trigger();  // the grad_ape finalisation may launch; it waits for this grid's end
     const int lanes = blockDim.y;
     const int x = threadIdx.x, y = threadIdx.y;
     const int j = (blockIdx.y * blockDim.x + x) * (2 * NW);
@@ -556,7 +558,8 @@ __global__ void __launch_bounds__(256) dape_finalize_kernel(const float *__restr
                                                             int n_partials, int64_t n,
                                                             float *__restrict__ dape)
 {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_wait();
+    pdl_trigger();
     const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t i = gt >> 5;
     const int t = (int)(gt & 31);
@@ -607,9 +610,7 @@ cudaError_t launch_dape_finalize(const float *partial, int n_partials, int64_t n
     cfg.gridDim = dim3((unsigned)((threads + 255) / 256), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, dape_finalize_kernel, partial, n_partials, n, dape);
@@ -638,8 +639,14 @@ static cudaError_t launch_fwd_small_t(const FwdParams &p, int num_sms, cudaStrea
     const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * num_sms;
     if (grid > resident)
         grid = resident;
-    fwd_small_kernel<RATIO, COFF><<<(unsigned)grid, kFwdThreads, 0, st>>>(a, static_cast<uint16_t *>(p.out));
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kFwdThreads, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fwd_small_kernel<RATIO, COFF>, a, static_cast<uint16_t *>(p.out));
 }
 
 cudaError_t launch_fwd_small(const FwdParams &p, int num_sms, cudaStream_t st)
@@ -694,13 +701,14 @@ static cudaError_t launch_bwd_small_t(const BwdParams &p, const SmallBwdPlan &pl
     cfg.blockDim = dim3(pl.threads_x, pl.lanes, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = pl.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, pl.rows_per_block, p.n_tokens,
                                        static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
                                        static_cast<uint16_t *>(p.dscore), partial);

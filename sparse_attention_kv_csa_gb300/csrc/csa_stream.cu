@@ -326,6 +326,8 @@ __global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG) fwd_stream_kernel(StreamArgs 
         mbar_init_fence();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
     if (warp == ncw) {
         if (lane == 0)
             produce<RATIO, COFF, false>(a, s, tc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
@@ -401,12 +403,6 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
     const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t C = (int64_t)COFF * a.head_dim;
-    const int R = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;
-    const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
-    const int rend = R < a.capacity ? R : a.capacity;  // padding rows carry no gradient
-    GradOut o{dkv, dscore, n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg)};
-    // Let the grad_ape finalisation grid launch now; it waits for this grid's end.
-    asm volatile("griddepcontrol.launch_dependents;");
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(smem_addr(&s.full[i]), 1);
@@ -415,6 +411,12 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
         mbar_init_fence();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();  // the grad_ape finalisation may launch; it waits for this grid's end
+    const int R = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;
+    const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
+    const int rend = R < a.capacity ? R : a.capacity;  // padding rows carry no gradient
+    GradOut o{dkv, dscore, n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg)};
 
     float2 acc[W][kNP];
 #pragma unroll
@@ -681,9 +683,15 @@ static cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl,
     cudaError_t e = blocks_for<RATIO, COFF>(pl, false, p.capacity, &blocks);
     if (e != cudaSuccess)
         return e;
-    fwd_stream_kernel<RATIO, COFF><<<dim3(blocks, pl.tiles), pl.threads, pl.smem, st>>>(
-        a, static_cast<uint16_t *>(p.out));
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, pl.tiles, 1);
+    cfg.blockDim = dim3(pl.threads, 1, 1);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<RATIO, COFF>, a, static_cast<uint16_t *>(p.out));
 }
 
 cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st)
@@ -725,13 +733,14 @@ static cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl,
     cfg.blockDim = dim3(pl.threads, 1, 1);
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = pl.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, bwd_stream_kernel<RATIO, COFF>, a, p.n_tokens,
                            static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
                            static_cast<uint16_t *>(p.dscore), partial);
