@@ -25,7 +25,7 @@
 //   added in ascending warp pairs and then by a fixed xor-shuffle tree over the
 //   threads of a column;  inv = 1/den rounded;  o = num * inv;  out = bf16(o).
 // Backward per valid k: p = e_k * inv;  grad_kv = bf16(g*p);
-//   ds = p*(g*kv - g*o);  grad_score = bf16(ds); grad_ape as in the other kernels
+//   ds = p*fma(g, kv, -g*o);  grad_score = bf16(ds); grad_ape as in the other kernels
 //   (per-thread sums over its rows, cluster merge in rank order, fixed-order
 //   finalisation).  Bitwise run-to-run deterministic: fixed chunks, fixed orders.
 //
@@ -88,7 +88,8 @@ struct Meta {
     int row;
     int real;
     int first;
-    int pad[2];
+    int last;  // the last block of its segment
+    int pad;
 };
 
 template <int COFF>
@@ -165,6 +166,7 @@ __device__ void r128_produce(const R128Args &a, const R128Smem<COFF> &s, const C
         m.row = row;
         m.real = rm.real;
         m.first = rm.first;
+        m.last = rm.real && row + 1 == __ldg(a.cc + rm.seg + 1);
         const bool load = BWD ? rm.real : true;
         const int p0 = (COFF == 2 && rm.first) ? 1 : 0;
         const uint32_t bytes =
@@ -503,7 +505,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
         uint32_t ph = 0;
         for (int row = blockIdx.x; row < rend; row += gridDim.x) {
             const bool ok = mbar_wait(smem_addr(&s.full[st]), ph, a.status);
-            Meta m = Meta{0, 0, row, 0, 1, {0, 0}};
+            Meta m = Meta{0, 0, row, 0, 1, 0, 0};
             if (ok)
                 m = s.meta[st];
             // rows below cu_seqlens_comp[0] are not real: no loads, no gradient
@@ -545,6 +547,11 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
             const float2 inv[2] = {make_float2(inv4.x, inv4.y), make_float2(inv4.z, inv4.w)};
             const float2 go[2] = {mul2(gg[0], make_float2(o4.x, o4.y)), mul2(gg[1], make_float2(o4.z, o4.w))};
             const float2 ngo[2] = {make_float2(-go[0].x, -go[0].y), make_float2(-go[1].x, -go[1].y)};
+            // window position k = c + NC*i sits at token t0 + k (part = k / ratio)
+            const int64_t t0 = m.base - (int64_t)(COFF - 1) * kR;
+            const int64_t lim = n_tokens - t0;  // positions k < lim hold a real token
+            uint16_t *pk_dkv = dkv + t0 * C + (int64_t)c * C + col;
+            uint16_t *pk_dsc = dscore + t0 * C + (int64_t)c * C + col;
 #pragma unroll
             for (int i = 0; i < kKC; ++i) {
                 if (!pos_valid<COFF>(c, i, first))
@@ -557,18 +564,17 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
                 for (int q = 0; q < 2; ++q) {
                     const float2 pk = mul2(cs.e[i][q], inv[q]);
                     dk[q] = f2_to_bf16x2(mul2(gg[q], pk));
-                    const float2 ds = mul2(pk, add2(mul2(gg[q], bf16x2_to_f2(kw[q])), ngo[q]));
+                    const float2 ds = mul2(pk, fma2(gg[q], bf16x2_to_f2(kw[q]), ngo[q]));
                     dsw[q] = f2_to_bf16x2(ds);
                     acc[i][q] = add2(acc[i][q], ds);
                 }
-                const int64_t tok = m.base + (int64_t)(part - (COFF - 1)) * kR + tk;
-                if (tok < n_tokens) {
-                    const int64_t gi = tok * C + (int64_t)part * a.head_dim + col;
-                    *reinterpret_cast<uint2 *>(dkv + gi) = make_uint2(dk[0], dk[1]);
-                    *reinterpret_cast<uint2 *>(dscore + gi) = make_uint2(dsw[0], dsw[1]);
+                if (c + G::NC * i < lim) {
+                    const int64_t off = (int64_t)(G::NC * i) * C + (int64_t)part * a.head_dim;
+                    *reinterpret_cast<uint2 *>(pk_dkv + off) = make_uint2(dk[0], dk[1]);
+                    *reinterpret_cast<uint2 *>(pk_dsc + off) = make_uint2(dsw[0], dsw[1]);
                 }
             }
-            if (m.row + 1 == __ldg(a.cc + m.seg + 1)) {  // last block of its segment
+            if (m.last) {  // last block of its segment
                 if (COFF == 2)  // own block's first-half columns: read by no row
                     r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, m.base, m.base + kR, n_tokens, c, false);
                 int64_t next = n_tokens;
