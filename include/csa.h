@@ -45,13 +45,14 @@
  * the ABI.  csa_last_error_message() gives a thread-local description of the
  * calling thread's last non-OK return.
  *
- * Supported set (csa_check_support): coff in {1, 2}; ratio == 4 with head_dim a
- * multiple of 8 in [8, 8192]; ratio == 128 with head_dim a multiple of 64 in
- * [64, 8192].  Numerics per ratio family (section Numerics): ratio 4 computes
- * every window in ascending position order (bitwise equal to a plain sequential
- * fp32 evaluation with the library's exp); ratio 128 sums the window in fixed
- * chunks (deterministic, equal to the sequential evaluation within final-bf16
- * rounding tolerance).
+ * Supported set (csa_check_support): coff in {1, 2}; ratio == 128 with head_dim a
+ * multiple of 64 in [64, 8192]; every other ratio in [1, 128] with head_dim a
+ * multiple of 8 in [8, 8192].  Numerics per ratio family (section Numerics): ratio
+ * 128 sums the window in fixed chunks with the hardware exp2 (deterministic, equal
+ * to the sequential evaluation within final-bf16 rounding tolerance); every other
+ * ratio (4 on its own kernels, the rest on the generic ones) computes each window
+ * in ascending position order with the library's exp, bitwise equal to a plain
+ * sequential fp32 evaluation.
  */
 #ifndef CSA_H_
 #define CSA_H_
@@ -135,7 +136,8 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * occupies 6 MiB on every GPU that loads the library, until the process exits.
  * A shape that needs more partial storage than the array holds is rejected with
  * CSA_ERR_TOO_LARGE before anything is launched (on a 152-SM GB300 every shape
- * fits except ratio 128 with coff 2 and head_dim above 6144).  No cudaMalloc,
+ * fits except ratio 128 with coff 2 and head_dim above 6144, and other ratios
+ * with ratio * coff * head_dim above 1572864).  No cudaMalloc,
  * cudaFree or other allocating call is made.
  *
  * Every call on a device shares the array and leaves its contents behind; each

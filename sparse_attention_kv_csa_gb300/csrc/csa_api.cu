@@ -105,8 +105,10 @@ int check_common(int32_t n_seg, int32_t ratio, int32_t coff, int32_t head_dim, i
         if (head_dim % 64 != 0 || head_dim > 8192)
             return fail(CSA_ERR_UNSUPPORTED,
                         "ratio 128 needs head_dim a multiple of 64 in [64, 8192] (got %d)", head_dim);
-    } else {
-        return fail(CSA_ERR_UNSUPPORTED, "ratio %d has no kernel (supported: 4, 128)", ratio);
+    } else if (ratio > 128 || head_dim % 8 != 0 || head_dim > 8192) {
+        return fail(CSA_ERR_UNSUPPORTED,
+                    "ratio %d needs ratio <= 128 and head_dim a multiple of 8 in [8, 8192] (got head_dim %d)",
+                    ratio, head_dim);
     }
     if ((int64_t)capacity * head_dim >= kInt32Limit)
         return fail(CSA_ERR_TOO_LARGE, "capacity * head_dim = %lld does not fit int32 offsets",
@@ -208,6 +210,8 @@ int csa_compress_fwd(const void *kv, const void *score, const float *ape, const 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (csa::r128_supported(ratio, coff, head_dim))
         e = csa::launch_fwd_r128(p, ds->status, st);
+    else if (ratio != 4)
+        e = csa::launch_fwd_generic(p, ds->num_sms, st);
     else if (csa::stream_supported(ratio, coff, head_dim))
         e = csa::launch_fwd_stream(p, csa::plan_stream(false, ratio, coff, head_dim, capacity, ds->num_sms),
                                    ds->status, st);
@@ -247,9 +251,11 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
     csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
     const bool r128 = csa::r128_supported(ratio, coff, head_dim);
-    const bool streamed = !r128 && csa::stream_supported(ratio, coff, head_dim);
+    const bool generic = !r128 && ratio != 4;
+    const bool streamed = !r128 && !generic && csa::stream_supported(ratio, coff, head_dim);
     csa::StreamPlan sp{};
     csa::SmallBwdPlan pl{};
+    csa::GenericPlan gp{};
     int64_t floats = 0;
     int r128_blocks = 0;
     if (r128) {
@@ -258,6 +264,9 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
         if (e != cudaSuccess)
             return cuda_fail(e, "backward plan");
         floats = (int64_t)partials * ratio * coff * head_dim;
+    } else if (generic) {
+        gp = csa::plan_generic(ratio, coff, head_dim, capacity, ds->num_sms);
+        floats = gp.partial_floats;
     } else if (streamed) {
         sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, ds->num_sms);
         floats = (int64_t)csa::stream_bwd_partials(sp, capacity) * ratio * coff * head_dim;
@@ -271,6 +280,8 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
         return cuda_fail(e, "backward workspace");
     if (r128)
         e = csa::launch_bwd_r128(p, static_cast<float *>(partial), r128_blocks, ds->status, st);
+    else if (generic)
+        e = csa::launch_bwd_generic(p, gp, static_cast<float *>(partial), st);
     else if (streamed)
         e = csa::launch_bwd_stream(p, sp, static_cast<float *>(partial), ds->status, st);
     else

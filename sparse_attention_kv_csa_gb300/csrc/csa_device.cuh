@@ -175,13 +175,14 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinte
 // visible (it returns at once after any other predecessor); a kernel reads and
 // writes no global memory before it.  pdl_trigger() then lets the next such
 // launch do the same.
+namespace csa {
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------- async copies, barriers
 // Shared-memory mbarriers and raw bulk copies (cp.async.bulk: contiguous global
 // bytes -> shared memory, completion counted on an mbarrier in bytes).
-namespace csa {
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {

@@ -96,6 +96,22 @@ cudaError_t launch_fwd_r128(const FwdParams &p, unsigned *status, cudaStream_t s
 cudaError_t r128_bwd_partials(int coff, int head_dim, int capacity, int *partials, int *blocks);
 cudaError_t launch_bwd_r128(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st);
 
+// Every other ratio in [1, 128] (thread per column pair, window walked from global
+// memory), head_dim % 8 == 0.
+struct GenericPlan {
+    int col_tiles;          // blocks along the columns (32 pairs each)
+    int lanes;              // rows walked side by side in a block (blockDim.y)
+    int groups;             // row groups = gridDim.x = grad_ape partials
+    int rows_per_group;     // contiguous output rows per group
+    size_t smem;            // backward shared memory (grad_ape slots)
+    int64_t partial_floats; // workspace floats
+    int num_sms;
+};
+bool generic_supported(int ratio, int coff, int head_dim);
+GenericPlan plan_generic(int ratio, int coff, int head_dim, int capacity, int num_sms);
+cudaError_t launch_fwd_generic(const FwdParams &p, int num_sms, cudaStream_t st);
+cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float *partial, cudaStream_t st);
+
 // Records a status and the thread-local message returned by csa_last_error_message().
 int fail_status(int status, const char *fmt, ...);
 SmallBwdPlan plan_bwd_small(int ratio, int coff, int head_dim, int capacity, int num_sms);

@@ -25,7 +25,8 @@
 
 // Scratch for the grad_ape partials: 1572864 floats = 6 MiB per GPU.  On a
 // 152-SM GB300 every shape fits except ratio 128 with coff 2 and head_dim above
-// 6144, which is rejected.
+// 6144, and other ratios with ratio * coff * head_dim above 1572864, which are
+// rejected.
 static constexpr size_t kScratchFloats = 1536u * 1024u;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 // Status word of the bounded waits of calls made through this entry point.
@@ -116,9 +117,11 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool r128 = csa::r128_supported(ratio, coff, head_dim);
-    const bool streamed = !r128 && csa::stream_supported(ratio, coff, head_dim);
+    const bool generic = !r128 && ratio != 4;
+    const bool streamed = !r128 && !generic && csa::stream_supported(ratio, coff, head_dim);
     csa::StreamPlan sp{};
     csa::SmallBwdPlan pl{};
+    csa::GenericPlan gp{};
     int64_t floats = 0;
     int r128_blocks = 0;
     if (r128) {
@@ -127,6 +130,9 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
         if (e != cudaSuccess)
             return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
         floats = (int64_t)partials * ratio * coff * head_dim;
+    } else if (generic) {
+        gp = csa::plan_generic(ratio, coff, head_dim, capacity, nd->num_sms);
+        floats = gp.partial_floats;
     } else if (streamed) {
         sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, nd->num_sms);
         int blocks = 0;
@@ -145,6 +151,8 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
                                 (long long)floats, (long long)kScratchFloats);
     if (r128)
         e = csa::launch_bwd_r128(p, nd->scratch, r128_blocks, nd->status, st);
+    else if (generic)
+        e = csa::launch_bwd_generic(p, gp, nd->scratch, st);
     else if (streamed)
         e = csa::launch_bwd_stream(p, sp, nd->scratch, nd->status, st);
     else

@@ -44,7 +44,7 @@ A16 = 1 << 20  # an aligned fake address; validation fails before it is used
 
 @pytest.mark.parametrize("kw,status", [
     (dict(coff=3), 1), (dict(ratio=0), 1), (dict(head_dim=0), 1), (dict(n_seg=-1), 1),
-    (dict(capacity=-1), 1), (dict(ratio=5), 2), (dict(head_dim=60), 2), (dict(head_dim=8200), 2),
+    (dict(capacity=-1), 1), (dict(ratio=129), 2), (dict(head_dim=60), 2), (dict(head_dim=8200), 2),
     (dict(capacity=1 << 30, head_dim=512), 4), (dict(cu=None), 1), (dict(kv=None), 1),
     (dict(out=A16 + 2), 3), (dict(ape=A16 + 4), 3), (dict(cu=A16 + 2), 3),
 ])
@@ -85,4 +85,8 @@ def test_check_support_surface():
     assert csa.csa_check_support(4, 2, 512, 3, 1) == 1        # fewer tokens than ratio
     assert csa.csa_check_support(4, 2, 512, 3, 0) == 0        # no rows: fine
     assert csa.csa_check_support(4, 2, 512, 1 << 21, 1) == 4  # 2^21 * 1024 >= 2^31
-    assert csa.csa_check_support(7, 2, 512, 100, 1) == 2
+    assert csa.csa_check_support(7, 2, 512, 100, 1) == 0      # generic ratios 1..128
+    assert csa.csa_check_support(1, 1, 8, 1, 1) == 0
+    assert csa.csa_check_support(129, 1, 512, 1000, 1) == 2   # no kernel beyond 128
+    assert csa.csa_check_support(7, 2, 500, 100, 1) == 2      # head_dim % 8
+    assert csa.csa_check_support(128, 1, 96, 1000, 1) == 2    # ratio 128: head_dim % 64

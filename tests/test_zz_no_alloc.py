@@ -91,3 +91,13 @@ def test_noalloc_rejects_shape_beyond_its_scratch(csa):
     assert "scratch" in str(ei.value)
     torch.cuda.synchronize()
     assert not dkv.any()
+
+
+def test_noalloc_generic_ratio_matches_backward(csa):
+    c = w.make_case("na_gen", 16, 2, 512, [4000, 37, 600], extra_rows=5, seed=8)
+    d = Dev(c)
+    want = run_bwd(d, csa)
+    for canary in (0xFFFF, 0x7FC1):
+        got = run_noalloc(d, csa, canary)
+        assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
+        assert np.array_equal(got[2].view(np.uint32), want[2].view(np.uint32))
