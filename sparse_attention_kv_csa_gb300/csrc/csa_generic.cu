@@ -4,7 +4,8 @@
 //
 // One thread owns a pair of adjacent columns j, j+1 of one output row and walks
 // the window three times (max; exp and sums; gradients), reading each position's
-// bf16 pair of score and kv and fp32 pair of APE straight from global memory: the
+// bf16 pair of score and kv and fp32 pair of APE straight from global memory, eight
+// positions' loads in flight at a time: the
 // window is too long for registers at large ratios and too short to amortise a
 // staged pipeline at small ones.  The repeated reads of a row's window hit L1/L2,
 // so DRAM traffic stays the algorithmic bytes.  The arithmetic is the library's
@@ -79,11 +80,35 @@ __device__ __forceinline__ Slot gen_slot(const GenArgs &a, const RowMap &rm, int
     return s;
 }
 
-__device__ __forceinline__ float2 gen_logit(const GenArgs &a, const Slot &s, int64_t C)
+// A batch of kGB consecutive window positions k0 .. k0 + kGB - 1, loaded before
+// any of them is used so that the loads are in flight together; the arithmetic
+// then takes them in ascending order.
+constexpr int kGB = 8;
+
+struct GenBatch {
+    uint32_t sw[kGB];  // score pair
+    uint32_t kw[kGB];  // kv pair (when loaded)
+    float2 ap[kGB];    // APE pair
+    unsigned valid;    // bit u: position k0 + u exists and is valid
+};
+
+template <bool KV>
+__device__ __forceinline__ void gen_fetch(const GenArgs &a, const RowMap &rm, int k0, int W, int j, int64_t C,
+                                          GenBatch &b)
 {
-    const uint32_t sw = __ldg(reinterpret_cast<const unsigned int *>(a.score + s.tok * C + s.col));
-    const float2 ap = __ldg(reinterpret_cast<const float2 *>(a.ape + (int64_t)s.arow * C + s.col));
-    return add2(bf16x2_to_f2(sw), ap);
+    b.valid = 0u;
+#pragma unroll
+    for (int u = 0; u < kGB; ++u) {
+        const int k = k0 + u;
+        if (k < W && gen_valid(a, rm, k)) {
+            b.valid |= 1u << u;
+            const Slot sl = gen_slot(a, rm, k, j);
+            b.sw[u] = __ldg(reinterpret_cast<const unsigned int *>(a.score + sl.tok * C + sl.col));
+            b.ap[u] = __ldg(reinterpret_cast<const float2 *>(a.ape + (int64_t)sl.arow * C + sl.col));
+            if (KV)
+                b.kw[u] = __ldg(reinterpret_cast<const unsigned int *>(a.kv + sl.tok * C + sl.col));
+        }
+    }
 }
 
 // Passes 1 and 2 of one row: m (NaN-propagating max), den and num.
@@ -92,24 +117,32 @@ __device__ __forceinline__ void gen_pool(const GenArgs &a, const RowMap &rm, int
 {
     const int W = a.coff * a.ratio;
     m = make_float2(-INFINITY, -INFINITY);
-    for (int k = 0; k < W; ++k) {
-        if (!gen_valid(a, rm, k))
-            continue;
-        const float2 s = gen_logit(a, gen_slot(a, rm, k, j), C);
-        m.x = max_nan(m.x, s.x);
-        m.y = max_nan(m.y, s.y);
+    for (int k0 = 0; k0 < W; k0 += kGB) {
+        GenBatch b;
+        gen_fetch<false>(a, rm, k0, W, j, C, b);
+#pragma unroll
+        for (int u = 0; u < kGB; ++u) {
+            if (!(b.valid >> u & 1u))
+                continue;
+            const float2 s = add2(bf16x2_to_f2(b.sw[u]), b.ap[u]);
+            m.x = max_nan(m.x, s.x);
+            m.y = max_nan(m.y, s.y);
+        }
     }
     const float2 negm = make_float2(-m.x, -m.y);
     den = make_float2(0.0f, 0.0f);
     num = make_float2(0.0f, 0.0f);
-    for (int k = 0; k < W; ++k) {
-        if (!gen_valid(a, rm, k))
-            continue;
-        const Slot sl = gen_slot(a, rm, k, j);
-        const float2 e = exp2lanes(add2(gen_logit(a, sl, C), negm));
-        const uint32_t kw = __ldg(reinterpret_cast<const unsigned int *>(a.kv + sl.tok * C + sl.col));
-        den = add2(den, e);
-        num = fma2(e, bf16x2_to_f2(kw), num);
+    for (int k0 = 0; k0 < W; k0 += kGB) {
+        GenBatch b;
+        gen_fetch<true>(a, rm, k0, W, j, C, b);
+#pragma unroll
+        for (int u = 0; u < kGB; ++u) {
+            if (!(b.valid >> u & 1u))
+                continue;
+            const float2 e = exp2lanes(add2(add2(bf16x2_to_f2(b.sw[u]), b.ap[u]), negm));
+            den = add2(den, e);
+            num = fma2(e, bf16x2_to_f2(b.kw[u]), num);
+        }
     }
 }
 
@@ -150,7 +183,7 @@ __device__ __forceinline__ void gen_zero(const GenArgs &a, uint16_t *dkv, uint16
     }
 }
 
-__global__ void __launch_bounds__(kGenBwdPairs * kGenBwdMaxLanes)
+__global__ void __launch_bounds__(kGenBwdPairs * kGenBwdMaxLanes, 2)
     bwd_generic_kernel(GenArgs a, int rows_per_group, int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out,
                        uint16_t *__restrict__ dkv, uint16_t *__restrict__ dscore, float *__restrict__ partial)
 {
@@ -193,19 +226,23 @@ __global__ void __launch_bounds__(kGenBwdPairs * kGenBwdMaxLanes)
         const float2 inv = make_float2(recip_den(den.x), recip_den(den.y));
         const float2 go = mul2(g, mul2(num, inv));
         const float2 ngo = make_float2(-go.x, -go.y), negm = make_float2(-m.x, -m.y);
-        for (int k = 0; k < W; ++k) {
-            if (!gen_valid(a, rm, k))
-                continue;
-            const Slot sl = gen_slot(a, rm, k, j);
-            const float2 e = exp2lanes(add2(gen_logit(a, sl, C), negm));
-            const float2 kvf =
-                bf16x2_to_f2(__ldg(reinterpret_cast<const unsigned int *>(a.kv + sl.tok * C + sl.col)));
-            const float2 pk = mul2(e, inv);
-            const float2 ds = mul2(pk, add2(mul2(g, kvf), ngo));
-            mine[k * TP] = add2(mine[k * TP], ds);
-            if (sl.tok < n_tokens) {
-                *reinterpret_cast<uint32_t *>(dkv + sl.tok * C + sl.col) = f2_to_bf16x2(mul2(g, pk));
-                *reinterpret_cast<uint32_t *>(dscore + sl.tok * C + sl.col) = f2_to_bf16x2(ds);
+        for (int k0 = 0; k0 < W; k0 += kGB) {
+            GenBatch b;
+            gen_fetch<true>(a, rm, k0, W, j, C, b);
+#pragma unroll
+            for (int u = 0; u < kGB; ++u) {
+                if (!(b.valid >> u & 1u))
+                    continue;
+                const Slot sl = gen_slot(a, rm, k0 + u, j);
+                const float2 e = exp2lanes(add2(add2(bf16x2_to_f2(b.sw[u]), b.ap[u]), negm));
+                const float2 pk = mul2(e, inv);
+                const float2 ds = mul2(pk, add2(mul2(g, bf16x2_to_f2(b.kw[u])), ngo));
+                float2 &ak = mine[(k0 + u) * TP];
+                ak = add2(ak, ds);
+                if (sl.tok < n_tokens) {
+                    *reinterpret_cast<uint32_t *>(dkv + sl.tok * C + sl.col) = f2_to_bf16x2(mul2(g, pk));
+                    *reinterpret_cast<uint32_t *>(dscore + sl.tok * C + sl.col) = f2_to_bf16x2(ds);
+                }
             }
         }
         if (r + 1 == __ldg(a.cc + rm.seg + 1)) {  // last block of its segment
