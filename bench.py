@@ -11,7 +11,8 @@ earlier and streams it from HBM (no flush).  `fwd` and `bwd` time each pass
 alone the same way (K calls back to back).  `e2e` is the same metric
 through the C ABI with pinned host buffers: host-to-device copies of the
 inputs, forward, backward and device-to-host copies of all outputs inside the
-timed region.
+timed region; consecutive steps overlap their copies and compute on three streams
+(two buffer sets), as a data pipeline would.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
 
@@ -256,10 +257,16 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_e2e(args, c, csa, dev, stream, world):
-    """Same step through the C ABI from pinned host buffers: H2D inputs, forward,
-    backward, D2H outputs, all inside the timed region."""
+    """Same step through the C ABI from pinned host buffers: every step copies its
+    inputs host-to-device, runs the forward and the backward, and copies all four
+    outputs device-to-host, all inside the timed region.  Consecutive steps overlap
+    as in a data pipeline: host-to-device copies, compute and device-to-host copies
+    each run on a stream of their own over two device buffer sets, ordered by events
+    (a step's compute waits for its inputs and for the copy-back of the outputs the
+    set last held; a set's inputs are refilled only after the compute that read them)."""
     import torch
     C = c.coff * c.head_dim
+    NB = 2
 
     def pin(a):
         a = np.ascontiguousarray(a)
@@ -267,39 +274,61 @@ def run_e2e(args, c, csa, dev, stream, world):
         return t.pin_memory()
 
     h_in = [pin(c.kv), pin(c.score), pin(c.ape), pin(c.cu_seqlens), pin(c.cu_seqlens_comp), pin(c.grad_out)]
-    d_in = [torch.empty_like(t, device=dev) for t in h_in]
-    d_out = [torch.empty((c.capacity, c.head_dim), dtype=torch.int16, device=dev),
-             torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev),
-             torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev),
-             torch.empty((c.ratio, C), dtype=torch.float32, device=dev)]
-    h_out = [torch.empty_like(t, device="cpu").pin_memory() for t in d_out]
+    d_in = [[torch.empty_like(t, device=dev) for t in h_in] for _ in range(NB)]
+
+    def outputs():
+        return [torch.empty((c.capacity, c.head_dim), dtype=torch.int16, device=dev),
+                torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev),
+                torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev),
+                torch.empty((c.ratio, C), dtype=torch.float32, device=dev)]
+
+    d_out = [outputs() for _ in range(NB)]
+    h_out = [[torch.empty_like(t, device="cpu").pin_memory() for t in d_out[0]] for _ in range(NB)]
     h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), stream, torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(NB)]    # set b's inputs are on the device
+    ev_used = [torch.cuda.Event() for _ in range(NB)]  # set b's compute is done
+    ev_out = [torch.cuda.Event() for _ in range(NB)]   # set b's outputs are back on the host
+    for evs in (ev_in, ev_used, ev_out):
+        for e in evs:
+            e.record(s_cmp)
 
-    def step():
-        for d, h in zip(d_in, h_in):
-            d.copy_(h, non_blocking=True)
-        kv, sc, ape, cu, cc, g = d_in
-        out, dkv, dsc, dape = d_out
-        csa.csa_compress_fwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity, out, stream)
+    def step(i):
+        b = i % NB
+        s_in.wait_event(ev_used[b])
+        with torch.cuda.stream(s_in):
+            for d, h in zip(d_in[b], h_in):
+                d.copy_(h, non_blocking=True)
+        ev_in[b].record(s_in)
+        s_cmp.wait_event(ev_in[b])
+        s_cmp.wait_event(ev_out[b])
+        kv, sc, ape, cu, cc, g = d_in[b]
+        out, dkv, dsc, dape = d_out[b]
+        csa.csa_compress_fwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity, out, s_cmp)
         csa.csa_compress_bwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity,
-                             c.n_tokens, g, dkv, dsc, dape, stream)
-        for h, d in zip(h_out, d_out):
-            h.copy_(d, non_blocking=True)
+                             c.n_tokens, g, dkv, dsc, dape, s_cmp)
+        ev_used[b].record(s_cmp)
+        s_out.wait_event(ev_used[b])
+        with torch.cuda.stream(s_out):
+            for h, d in zip(h_out[b], d_out[b]):
+                h.copy_(d, non_blocking=True)
+        ev_out[b].record(s_out)
 
-    for _ in range(max(3, args.warmup)):
-        step()
+    for i in range(max(3, args.warmup)):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     k = max(3, min(args.steps, 20))
-    e0.record(stream)
-    for _ in range(k):
-        step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(k):
+        step(i)
+    e1.record(s_out)  # after the last copy-back, which follows every earlier operation
     torch.cuda.synchronize()
     ms = max_over_ranks([e0.elapsed_time(e1) / k])[0]
     return {"value": world * c.n_tokens / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "H2D, compute and D2H of consecutive steps on three streams, two buffer sets"}
 
 
 # ------------------------------------------------------- CPU oracle leg
