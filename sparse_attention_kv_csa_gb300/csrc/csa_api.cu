@@ -150,6 +150,32 @@ int check_ptr(const void *p, const char *name, uintptr_t align)
 
 namespace csa {
 
+cudaError_t allow_max_smem(const void *fn)
+{
+    static std::mutex mu;
+    static int devs[256];
+    static const void *fns[256];
+    static int n = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> g(mu);
+    for (int i = 0; i < n; ++i)
+        if (devs[i] == dev && fns[i] == fn)
+            return cudaSuccess;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess && n < 256) {
+        devs[n] = dev;
+        fns[n] = fn;
+        ++n;
+    }
+    return e;
+}
+
 int fail_status(int status, const char *fmt, ...)
 {
     va_list ap;

@@ -322,8 +322,7 @@ cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float 
     GenArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
               p.cu_seqlens_comp, p.n_seg, p.ratio, p.coff, p.head_dim, p.capacity};
     if (pl.smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)pl.smem);
+        cudaError_t e = allow_max_smem(reinterpret_cast<const void *>(bwd_generic_kernel));
         if (e != cudaSuccess)
             return e;
     }

@@ -112,6 +112,11 @@ GenericPlan plan_generic(int ratio, int coff, int head_dim, int capacity, int nu
 cudaError_t launch_fwd_generic(const FwdParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float *partial, cudaStream_t st);
 
+// Raises a kernel's dynamic shared-memory limit (a per-function attribute shared
+// by all its launch configurations) to the current device's maximum, once per
+// (device, kernel).
+cudaError_t allow_max_smem(const void *fn);
+
 // Records a status and the thread-local message returned by csa_last_error_message().
 int fail_status(int status, const char *fmt, ...);
 SmallBwdPlan plan_bwd_small(int ratio, int coff, int head_dim, int capacity, int num_sms);

@@ -692,7 +692,7 @@ static cudaError_t launch_bwd_small_t(const BwdParams &p, const SmallBwdPlan &pl
                 p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity};
     auto kern = bwd_small_kernel<RATIO, COFF>;
     if (pl.smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+        cudaError_t e = allow_max_smem(reinterpret_cast<const void *>(kern));
         if (e != cudaSuccess)
             return e;
     }

@@ -288,3 +288,16 @@ def test_r128_small_layouts(csa, coff, head_dim):
             t[1] += b
             t[2] += n
     assert_counts([tuple(t) for t in total])
+
+
+def test_interleaved_head_dims_keep_working(csa):
+    """Plans of different head_dims need different shared memory on the same
+    kernel; launching a larger one after a smaller one must still work (the
+    kernel's shared-memory limit is a per-function attribute)."""
+    for i, head_dim in enumerate([512, 128, 384, 512, 128, 1024]):
+        c = w.make_case("inter", 4, 2, head_dim, [70, 33], extra_rows=1, seed=40 + i)
+        d = Dev(c)
+        assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))
+        dkv, dsc, _ = run_bwd(d, csa)
+        want = oracle.case_bwd_f32(c)
+        assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
