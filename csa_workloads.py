@@ -189,6 +189,9 @@ SPECS = {
                                       kv_scale=64.0, grad_scale=64.0),
     "stress_overflow": lambda seed=0: dict(name="stress_overflow", ratio=4, coff=2, head_dim=512,
                                            seqlens=[131072]),
+    # ratio 128 with the overlapping window (coff 2, window 256), head_dim 512
+    "r128c2d512_4x32768": lambda seed=0: dict(name="r128c2d512_4x32768", ratio=128, coff=2, head_dim=512,
+                                              seqlens=[32768] * 4),
     # a ratio served by the generic kernels: ratio 16, coff 2, head_dim 512,
     # 8 segments of 4096 tokens (2048 rows), 64 padding rows
     "r16c2d512_8x4096": lambda seed=0: dict(name="r16c2d512_8x4096", ratio=16, coff=2, head_dim=512,

@@ -99,7 +99,7 @@ cudaError_t launch_bwd_r128(const BwdParams &p, float *partial, int blocks, unsi
 // Every other ratio in [1, 128] (thread per column pair, window walked from global
 // memory), head_dim % 8 == 0.
 struct GenericPlan {
-    int col_tiles;          // blocks along the columns (32 pairs each)
+    int col_tiles;          // blocks along the columns (16 groups of 4 columns each)
     int lanes;              // rows walked side by side in a block (blockDim.y)
     int groups;             // row groups = gridDim.x = grad_ape partials
     int rows_per_group;     // contiguous output rows per group

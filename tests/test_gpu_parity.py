@@ -265,6 +265,15 @@ def test_r128_workload_tolerance_and_determinism(csa):
     assert np.array_equal(b[2].view(np.uint32), dape.view(np.uint32))
 
 
+def test_r128_overlapping_window_workload(csa):
+    """ratio 128, coff 2 (window 256), 4 x 32768 tokens, head_dim 512."""
+    c = w.WORKLOADS["r128c2d512_4x32768"]()
+    (out, dkv, dsc, dape), counts = tolerance_counts(c, csa)
+    assert_counts(counts)
+    d = Dev(c)
+    assert np.array_equal(run_fwd(d, csa, canary=0x7FC1), out)
+
+
 R128_LAYOUTS = [[2400, 128, 5, 8000], [127], [128], [129, 0, 2048], [5120], [3, 5600, 2]]
 
 
