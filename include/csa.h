@@ -35,6 +35,15 @@
  * is a cudaStream_t (NULL = the legacy default stream).  Calls are asynchronous:
  * no call synchronises the device or reads device memory on the host.
  *
+ * Launch order: every kernel is launched as a programmatic dependent of its stream
+ * predecessor (CUDA programmatic dependent launch) and waits for that predecessor
+ * to complete before it reads or writes any global memory, so stream order holds
+ * after any kind of predecessor.  Its blocks may become resident early, while the
+ * predecessor drains.  A caller's own kernel launched with the programmatic
+ * stream-serialization attribute right after a call must likewise wait
+ * (griddepcontrol.wait / cudaGridDependencySynchronize) before using the call's
+ * outputs; plain launches need nothing.
+ *
  * Trusted device contents: the offsets in cu_seqlens / cu_seqlens_comp are not
  * validated (that would need a device-to-host read).  The caller guarantees the
  * relations above, capacity >= cu_seqlens_comp[n_seg], and that kv / score hold at

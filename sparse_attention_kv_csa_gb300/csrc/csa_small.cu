@@ -18,7 +18,7 @@
 // invalid positions are skipped, valid ones taken in ascending k):
 //   s_k = score + ape;  m = max_k s_k (NaN-propagating);  e_k = exp(s_k - m)
 //   den = ((+0 + e_0) + e_1) + ...;  num = fma(e_k, kv_k, num) from +0
-//   inv = rcp.rn(den);  o = num * inv;  out = bf16_rn(o)
+//   inv = 1/den rounded to nearest (recip_den);  o = num * inv;  out = bf16_rn(o)
 // Backward, per valid k, with g = grad_out:
 //   go = g*o;  p = e_k*inv;  grad_kv = bf16(g*p);  ds = p*(g*kv - go);
 //   grad_score = bf16(ds);  ds is summed into this thread's grad_ape partial.

@@ -5,7 +5,7 @@
 // Compressor", cuDNN frontend docs, sections Semantics and Numerics): window
 // positions in ascending k, invalid ones skipped; s = score + ape; NaN-propagating
 // max; e = exp(s - m) with the library's exp; den and num accumulated in ascending
-// k; inv = rcp.rn(den); out = bf16(num * inv); backward p = e*inv,
+// k; inv = 1/den rounded to nearest; out = bf16(num * inv); backward p = e*inv,
 // grad_kv = bf16(g*p), ds = p*(g*kv - g*o).  Results are bitwise those of
 // csa_small.cu.
 //
@@ -15,8 +15,9 @@
 //     output row reads -- each (token, half) is one contiguous run of TC*2 bytes --
 //     and, in the backward, the grad_out row; completion is counted in bytes on the
 //     stage's "full" mbarrier;
-//   * consumer warps: thread t owns columns [c0 + 4t, c0 + 4t + 4) of the block's
-//     column tile for every row, so its APE values stay in registers; it waits on
+//   * consumer warps: thread t owns columns [c0 + 2*kNP*t, c0 + 2*kNP*(t + 1)) of
+//     the block's column tile (kNP fp32 pairs, two by default) for every row, so
+//     its APE values stay in registers; it waits on
 //     the stage's "full" barrier, computes from shared memory, writes its outputs
 //     and releases the stage on the "empty" barrier.
 // Every wait is bounded in time; on expiry a timeout is recorded in the status
