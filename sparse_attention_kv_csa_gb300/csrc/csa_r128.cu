@@ -670,7 +670,7 @@ R128Plan r128_plan(bool bwd, int head_dim)
     using G = Geo<COFF>;
     R128Plan pl;
     pl.stage_bytes = (G::WIN_BYTES + (bwd ? G::TC * 2 : 0) + 1023) / 1024 * 1024;
-    pl.stages = 2;
+    pl.stages = bwd ? 4 : 2;  // the backward runs one block per SM: a deeper ring fits (measured on coff 2)
     pl.threads = G::THREADS;
     pl.tiles = head_dim / G::TC;
     pl.cluster = bwd ? CSA_R128_BWD_CLUSTER : 1;
