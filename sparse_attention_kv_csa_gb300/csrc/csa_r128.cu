@@ -53,6 +53,15 @@ namespace {
 constexpr int kR = 128;  // ratio
 constexpr int kKC = 8;   // window positions per chunk (per thread)
 
+// Backward layout per window form.  coff 1: APE and the kv words in registers,
+// the stage released as soon as it is read, one block per SM (registers), a
+// four-stage ring.  coff 2 (twice the column tiles per row): "lean" -- APE from a
+// shared tile, kv read again from the stage, which stays held until the row's
+// gradients are written -- so that two blocks fit per SM.  Each measured faster
+// for its form on GB300.
+template <int COFF>
+constexpr bool kBwdLean = COFF == 2;
+
 template <int COFF>
 struct Geo {
     static constexpr int TC = 64 / COFF;      // columns per block tile
@@ -98,22 +107,24 @@ struct R128Smem {
     float *mx;   // [2][CW][RS]  warp maxima
     float *den;  // [2][CW][RS]  warp sums
     float *num;  // [2][CW][RS]
-    float *fin;  // [2][2][TC]  (inv, g*o) for the backward
+    float *fin;  // [2][2][TC]  (inv, o) for the backward
+    float *apet; // [W][TC]  the backward's APE tile (null in the forward)
     Meta *meta;
     uint64_t *full;
     uint64_t *empty;
 };
 
 template <int COFF>
-__host__ __device__ size_t r128_smem_bytes(int stages, int stage_bytes)
+__host__ __device__ size_t r128_smem_bytes(int stages, int stage_bytes, bool ape_tile)
 {
     using G = Geo<COFF>;
-    return (size_t)stages * stage_bytes + 3 * 2 * G::CW * G::RS * 4 + 2 * 2 * G::TC * 4 + sizeof(Meta) * stages +
-           16 * stages + 16;
+    return (size_t)stages * stage_bytes + 3 * 2 * G::CW * G::RS * 4 + 2 * 2 * G::TC * 4 +
+           (ape_tile ? (size_t)G::W * G::TC * 4 : 0) + sizeof(Meta) * stages + 16 * stages + 16;
 }
 
 template <int COFF>
-__device__ __forceinline__ R128Smem<COFF> r128_carve(unsigned char *base, int stages, int stage_bytes)
+__device__ __forceinline__ R128Smem<COFF> r128_carve(unsigned char *base, int stages, int stage_bytes,
+                                                     bool ape_tile)
 {
     using G = Geo<COFF>;
     R128Smem<COFF> s;
@@ -123,7 +134,8 @@ __device__ __forceinline__ R128Smem<COFF> r128_carve(unsigned char *base, int st
     s.den = s.mx + 2 * G::CW * G::RS;
     s.num = s.den + 2 * G::CW * G::RS;
     s.fin = s.num + 2 * G::CW * G::RS;
-    p = reinterpret_cast<unsigned char *>(s.fin + 2 * 2 * G::TC);
+    s.apet = ape_tile ? s.fin + 2 * 2 * G::TC : nullptr;
+    p = reinterpret_cast<unsigned char *>(s.fin + 2 * 2 * G::TC + (ape_tile ? G::W * G::TC : 0));
     s.meta = reinterpret_cast<Meta *>(p);
     s.full = reinterpret_cast<uint64_t *>(s.meta + stages);
     s.empty = s.full + stages;
@@ -254,15 +266,50 @@ __device__ __forceinline__ float ex2_fast(float x)
     return y;
 }
 
+// Backward: s = score + ape for the thread's positions, APE from the block's tile
+// (kv is read from the stage again where it is needed).
+template <int COFF>
+__device__ __forceinline__ void r128_load_s(const unsigned char *stage, const float *apet, int c, int g,
+                                            bool first, ChunkState &cs)
+{
+#pragma unroll
+    for (int i = 0; i < kKC; ++i) {
+        if (!pos_valid<COFF>(c, i, first))
+            continue;
+        int part, tok;
+        position<COFF>(c, i, part, tok);
+        const int off = tok * Geo<COFF>::TC * 2 + 8 * g;
+        const uint2 sw = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(1, part) + off);
+        const float4 av =
+            *reinterpret_cast<const float4 *>(apet + (size_t)(c + Geo<COFF>::NC * i) * Geo<COFF>::TC + 4 * g);
+        cs.e[i][0] = add2(bf16x2_to_f2(sw.x), make_float2(av.x, av.y));
+        cs.e[i][1] = add2(bf16x2_to_f2(sw.y), make_float2(av.z, av.w));
+    }
+}
+
+// kv words of window position i of the thread: from the registers the forward
+// filled, or (KV_STAGE, the backward) from the stage.
+template <int COFF, bool KV_STAGE>
+__device__ __forceinline__ uint2 r128_kv(const ChunkState &cs, const unsigned char *stage, int c, int g, int i)
+{
+    if constexpr (KV_STAGE) {
+        int part, tok;
+        position<COFF>(c, i, part, tok);
+        return *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(0, part) + tok * Geo<COFF>::TC * 2 + 8 * g);
+    } else {
+        return cs.kv[i];
+    }
+}
+
 // The two merge phases of one row.  Every consumer thread calls this once per
 // row.  The first barrier also votes on `ok` (the thread's wait for the row's
 // data succeeded): if any thread failed, all return false together before the
 // second barrier.  `have`: the row has data (cs loaded).  On true: cs.e holds e_k
 // of the thread's valid positions, and each warp's sums over its chunks are in
 // the merge buffers for r128_final.
-template <int COFF>
+template <int COFF, bool KV_STAGE>
 __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int c, int g, bool ok, bool have,
-                                          bool first, ChunkState &cs)
+                                          bool first, ChunkState &cs, const unsigned char *stage)
 {
     using G = Geo<COFF>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -307,7 +354,8 @@ __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int 
     for (int i = 0; i < kKC; ++i) {
         if (!have || !pos_valid<COFF>(c, i, first))
             continue;
-        const uint32_t kw[2] = {cs.kv[i].x, cs.kv[i].y};
+        const uint2 kv = r128_kv<COFF, KV_STAGE>(cs, stage, c, g, i);
+        const uint32_t kw[2] = {kv.x, kv.y};
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const float2 x = fma2(cs.e[i][q], splat(kLog2eF), nml[q]);
@@ -390,11 +438,11 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
 {
     using G = Geo<COFF>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // TMA tensor destinations need 128-byte alignment: align the base by hand
-    // (the plan reserves 1 KB of slack for this).
+    // TMA tensor destinations need 128-byte alignment; the base is aligned to 1 KB
+    // by hand (the plan reserves 1 KB of slack for this).
     unsigned char *smem_base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                                  ~uintptr_t(1023));
-    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes);
+    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes, false);
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     r128_init<COFF>(s, a.stages);
@@ -423,7 +471,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
             st = 0;
             ph ^= 1u;
         }
-        if (!r128_pool<COFF>(s, buf, c, g, ok, ok, first, cs))
+        if (!r128_pool<COFF, false>(s, buf, c, g, ok, ok, first, cs, nullptr))
             break;
         {
             int j;
@@ -459,18 +507,19 @@ __device__ __forceinline__ void r128_zero_tokens(uint16_t *dkv, uint16_t *dscore
 }
 
 template <int COFF>
-__global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
+__global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
     bwd_r128_kernel(R128Args a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
                     int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
                     uint16_t *__restrict__ dscore, float *__restrict__ partial)
 {
     using G = Geo<COFF>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // TMA tensor destinations need 128-byte alignment: align the base by hand
-    // (the plan reserves 1 KB of slack for this).
+    // TMA tensor destinations need 128-byte alignment; the base is aligned to 1 KB
+    // by hand (the plan reserves 1 KB of slack for this).
     unsigned char *smem_base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                                  ~uintptr_t(1023));
-    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes);
+    constexpr bool LEAN = kBwdLean<COFF>;
+    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes, LEAN);
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t C = (int64_t)COFF * a.head_dim;
@@ -500,7 +549,18 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
             r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, 0, lead, n_tokens, c, true);
         }
         float2 ap[kKC][2];
-        r128_load_ape<COFF>(a, c, col, ap);
+        if constexpr (LEAN) {
+            // the block's APE tile [window position][tile column], read once
+            for (int v = threadIdx.x; v < G::W * G::TC / 4; v += G::CT) {
+                const int k = v / (G::TC / 4), c4 = v - k * (G::TC / 4);
+                const int part = k / kR, tk = k - part * kR;
+                *reinterpret_cast<float4 *>(s.apet + (size_t)v * 4) = __ldg(reinterpret_cast<const float4 *>(
+                    a.ape + (int64_t)tk * C + (int64_t)part * a.head_dim + c0 + 4 * c4));
+            }
+            named_barrier(1, G::CT);
+        } else {
+            r128_load_ape<COFF>(a, c, col, ap);
+        }
         int st = 0, buf = 0;
         uint32_t ph = 0;
         for (int row = blockIdx.x; row < rend; row += gridDim.x) {
@@ -510,21 +570,29 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
                 m = s.meta[st];
             // rows below cu_seqlens_comp[0] are not real: no loads, no gradient
             const bool first = m.first || !m.real;
+            const int st_row = st;
             const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
             ChunkState cs;
-            if (ok && m.real)
-                r128_load<COFF>(stage, c, g, first, ap, cs);
+            if (ok && m.real) {
+                if constexpr (LEAN)
+                    r128_load_s<COFF>(stage, s.apet, c, g, first, cs);
+                else
+                    r128_load<COFF>(stage, c, g, first, ap, cs);
+            }
             uint2 gw = make_uint2(0u, 0u);
             if (ok && m.real)
                 gw = *reinterpret_cast<const uint2 *>(stage + G::WIN_BYTES + 8 * g);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_addr(&s.empty[st]));
+            if constexpr (!LEAN) {  // everything the row needs is in registers now
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&s.empty[st_row]));
+            }
             if (++st == a.stages) {
                 st = 0;
                 ph ^= 1u;
             }
-            if (!r128_pool<COFF>(s, buf, c, g, ok, ok && m.real, first, cs))
+            // lean: the stage stays held until the gradients below have read kv from it
+            if (!r128_pool<COFF, LEAN>(s, buf, c, g, ok, ok && m.real, first, cs, stage))
                 break;
             const float2 gg[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
             float *fin = s.fin + (size_t)buf * 2 * G::TC;
@@ -540,8 +608,14 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
             }
             named_barrier(1, G::CT);
             buf ^= 1;
-            if (!m.real)
+            if (!m.real) {
+                if constexpr (LEAN) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(smem_addr(&s.empty[st_row]));
+                }
                 continue;
+            }
             const float4 inv4 = *reinterpret_cast<const float4 *>(fin + 4 * g);
             const float4 o4 = *reinterpret_cast<const float4 *>(fin + G::TC + 4 * g);
             const float2 inv[2] = {make_float2(inv4.x, inv4.y), make_float2(inv4.z, inv4.w)};
@@ -558,7 +632,8 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
                     continue;
                 int part, tk;
                 position<COFF>(c, i, part, tk);
-                const uint32_t kw[2] = {cs.kv[i].x, cs.kv[i].y};
+                const uint2 kv = r128_kv<COFF, LEAN>(cs, stage, c, g, i);
+                const uint32_t kw[2] = {kv.x, kv.y};
                 uint32_t dk[2], dsw[2];
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -573,6 +648,11 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 1)
                     *reinterpret_cast<uint2 *>(pk_dkv + off) = make_uint2(dk[0], dk[1]);
                     *reinterpret_cast<uint2 *>(pk_dsc + off) = make_uint2(dsw[0], dsw[1]);
                 }
+            }
+            if constexpr (LEAN) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&s.empty[st_row]));
             }
             if (m.last) {  // last block of its segment
                 if (COFF == 2)  // own block's first-half columns: read by no row
@@ -670,16 +750,20 @@ R128Plan r128_plan(bool bwd, int head_dim)
     using G = Geo<COFF>;
     R128Plan pl;
     pl.stage_bytes = (G::WIN_BYTES + (bwd ? G::TC * 2 : 0) + 1023) / 1024 * 1024;
-    pl.stages = bwd ? 4 : 2;  // the backward runs one block per SM: a deeper ring fits (measured on coff 2)
+    const bool tile = bwd && kBwdLean<COFF>;
+    // two blocks per SM (forward, lean backward): two stages; one block per SM
+    // (register-resident backward): a four-stage ring fits
+    pl.stages = bwd && !tile ? 4 : 2;
     pl.threads = G::THREADS;
     pl.tiles = head_dim / G::TC;
-    pl.cluster = bwd ? CSA_R128_BWD_CLUSTER : 1;
-    pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes) + 1024;  // + alignment slack
+    // lean backward: pairs of blocks merge their grad_ape partials (half as many)
+    pl.cluster = bwd ? (tile ? 2 : CSA_R128_BWD_CLUSTER) : 1;
+    pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes, tile) + 1024;  // + alignment slack
     if (bwd) {  // grad_ape staging reuses the stages: make sure it fits
         const size_t red = (size_t)kR * COFF * G::TC * sizeof(float);
         if ((size_t)pl.stages * pl.stage_bytes < red)
             pl.stages = (int)((red + pl.stage_bytes - 1) / pl.stage_bytes);
-        pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes) + 1024;
+        pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes, tile) + 1024;
     }
     return pl;
 }
@@ -839,7 +923,8 @@ cudaError_t r128_bwd_partials(int coff, int head_dim, int capacity, int *partial
 {
     cudaError_t e = coff == 2 ? r128_bwd_blocks_t<2>(head_dim, capacity, blocks)
                               : r128_bwd_blocks_t<1>(head_dim, capacity, blocks);
-    *partials = *blocks / CSA_R128_BWD_CLUSTER;
+    const int cluster = coff == 2 ? r128_plan<2>(true, head_dim).cluster : r128_plan<1>(true, head_dim).cluster;
+    *partials = *blocks / cluster;
     return e;
 }
 
