@@ -165,9 +165,13 @@ cudaError_t allow_max_smem(const void *fn)
         if (devs[i] == dev && fns[i] == fn)
             return cudaSuccess;
     int optin = 0;
+    cudaFuncAttributes fa;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = cudaFuncGetAttributes(&fa, fn);
+    if (e == cudaSuccess)  // the device maximum less the kernel's static shared memory
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - static_cast<int>(fa.sharedSizeBytes));
     if (e == cudaSuccess && n < 256) {
         devs[n] = dev;
         fns[n] = fn;

@@ -789,10 +789,7 @@ cudaError_t r128_blocks(const R128Plan &pl, bool bwd, int rows, int *out)
                 resident = cache_val[i];
     }
     if (resident < 0) {
-        int optin = 0;  // the function-wide limit: the device maximum, whatever this plan needs
-        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = allow_max_smem(fn);  // the function-wide limit: the device maximum, whatever this plan needs
         if (e != cudaSuccess)
             return e;
         if (pl.cluster > 1) {

@@ -623,10 +623,7 @@ static cudaError_t query_resident(const ResidentKey &k, int *resident)
     // The kernel's dynamic shared-memory limit is a per-function attribute shared by
     // every configuration: raise it to the device maximum (not to this plan's size,
     // which a later plan of another head_dim could undercut).
-    int optin = 0;
-    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, k.dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    cudaError_t e = allow_max_smem(k.fn);
     if (e != cudaSuccess)
         return e;
     if (k.cluster > 1) {
