@@ -1,6 +1,7 @@
 """CUDA-graph capture ("CSA Fused Compressor", section CUDA graphs: warm up each
 configuration, pass a static capacity): forward and backward captured once on a
-stream and replayed give the eager results bit for bit, for both ratio families."""
+stream and replayed give the eager results bit for bit, for every kernel family
+(ratio 4 pipelined and register-window, ratio 128 both window forms, generic ratios)."""
 import numpy as np
 import pytest
 
@@ -11,7 +12,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("ratio,coff,head_dim,lens", [(4, 2, 512, [4096, 37, 3]), (4, 2, 64, [300, 9]),
-                                                      (128, 1, 512, [4096, 300]), (128, 2, 128, [1000])])
+                                                      (128, 1, 512, [4096, 300]), (128, 2, 128, [1000]),
+                                                      (16, 2, 512, [900, 17]), (7, 1, 64, [300, 5])])
 def test_capture_and_replay_bitwise(ratio, coff, head_dim, lens):
     import torch
     import sparse_attention_kv_csa_gb300 as csa
