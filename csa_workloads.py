@@ -192,6 +192,22 @@ SPECS = {
     # ratio 128 with the overlapping window (coff 2, window 256), head_dim 512
     "r128c2d512_4x32768": lambda seed=0: dict(name="r128c2d512_4x32768", ratio=128, coff=2, head_dim=512,
                                               seqlens=[32768] * 4),
+    # a head_dim that is not a multiple of 128 (register-window kernels): ratio 4,
+    # coff 2, head_dim 64, 32 segments of 4096 tokens
+    "r4c2d64_32x4096": lambda seed=0: dict(name="r4c2d64_32x4096", ratio=4, coff=2, head_dim=64,
+                                           seqlens=[4096] * 32),
+    # head_dim 128 (the page's other head size), ratio 4, coff 2, 32 x 4096 tokens
+    "r4c2d128_32x4096": lambda seed=0: dict(name="r4c2d128_32x4096", ratio=4, coff=2, head_dim=128,
+                                            seqlens=[4096] * 32),
+    # head_dim 256, ratio 4, coff 2, 16 x 4096 tokens
+    "r4c2d256_16x4096": lambda seed=0: dict(name="r4c2d256_16x4096", ratio=4, coff=2, head_dim=256,
+                                            seqlens=[4096] * 16),
+    # the own-block window (coff 1): ratio 4, head_dim 512, 16 x 4096 tokens
+    "r4c1d512_16x4096": lambda seed=0: dict(name="r4c1d512_16x4096", ratio=4, coff=1, head_dim=512,
+                                            seqlens=[4096] * 16),
+    # head_dim 128 at ratio 128, coff 1, 4 x 131072 tokens
+    "r128c1d128_4x131072": lambda seed=0: dict(name="r128c1d128_4x131072", ratio=128, coff=1, head_dim=128,
+                                               seqlens=[131072] * 4),
     # a ratio served by the generic kernels: ratio 16, coff 2, head_dim 512,
     # 8 segments of 4096 tokens (2048 rows), 64 padding rows
     "r16c2d512_8x4096": lambda seed=0: dict(name="r16c2d512_8x4096", ratio=16, coff=2, head_dim=512,

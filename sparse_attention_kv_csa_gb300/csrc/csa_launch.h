@@ -71,6 +71,8 @@ cudaError_t launch_dape_finalize(const float *partial, int n_partials, int64_t n
 struct StreamPlan {
     int tc;              // columns per thread block tile (consumer threads x 4)
     int tiles;           // head_dim / tc (gridDim.y)
+    int row_lanes;       // rows in flight per block (tc / 128 column warps each)
+    bool whole;          // stage whole token rows (one column tile)
     int threads;         // consumer warps + one producer warp, x 32
     int stage_bytes;     // bytes per ring stage
     int stages;          // ring depth

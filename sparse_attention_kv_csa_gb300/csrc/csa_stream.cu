@@ -33,6 +33,9 @@
 namespace cg = cooperative_groups;
 
 // Ring sizes (bytes of stages per block) and the backward's cluster size.
+#ifndef CSA_STREAM_WHOLE_MAX_D  // widest coff-2 head staged as whole rows
+#define CSA_STREAM_WHOLE_MAX_D 256
+#endif
 #ifndef CSA_STREAM_FWD_BUDGET
 #define CSA_STREAM_FWD_BUDGET (64 * 1024)
 #endif
@@ -125,10 +128,53 @@ struct StreamArgs {
     int n_seg;
     int head_dim;
     int capacity;
-    int stages;        // ring depth
+    int stages;        // ring depth (a multiple of row_lanes)
     int stage_bytes;   // bytes per stage (multiple of 128)
     unsigned *status;  // caller-visible status word
+    int tc;            // columns of the block's tile
+    int row_lanes;     // rows in flight per block: groups of tc / (32 * 2 * kNP) warps
+    int rw;            // elements per staged token row: tc, or C for whole rows
+    int pcol;          // whole rows: head_dim (part p's data at column p * head_dim of a row); tiled: 0
 };
+
+// Staging of a window.  Tiled (rw = tc): per token of each part, the tile's
+// columns of that part, 2 * COFF * RATIO copies of tc elements.  Whole rows (one
+// column tile, rw = C): per part, the RATIO whole token rows of its block, one
+// contiguous copy of RATIO * C elements per array; coff 2 then also stages the
+// half of each row the window does not use (the neighbouring row reads it), in
+// exchange for 8x fewer, larger copies, which narrow heads need to keep the one
+// issuing thread ahead of the consumers.
+
+// Consumer warp w of a block works on column group w % (tc / kColsPerWarp) of the
+// tile and on row lane w / (tc / kColsPerWarp): the block's j-th row (in the
+// producer's order) goes to lane j % row_lanes, in ring slot j % stages.  With
+// stages a multiple of row_lanes every slot always serves the same lane, so no
+// consumer ever waits on a slot more than one phase ahead.
+struct Lanes {
+    int cols;  // column-group warps per row
+    int lane;  // this warp's row lane
+    int lc;    // this thread's first column in the tile
+};
+
+// Next slot of a row lane: `step` slots on, the phase flipping on each wrap
+// (stages is a multiple of step).
+__device__ __forceinline__ void ring_next(int &st, uint32_t &ph, int step, int stages)
+{
+    st += step;
+    if (st >= stages) {
+        st -= stages;
+        ph ^= 1u;
+    }
+}
+
+__device__ __forceinline__ Lanes lanes_of(const StreamArgs &a, int warp, int lane)
+{
+    Lanes l;
+    l.cols = a.tc / kColsPerWarp;
+    l.lane = warp / l.cols;
+    l.lc = ((warp % l.cols) * 32 + lane) * kCPT;
+    return l;
+}
 
 struct StageMeta {
     int64_t base;
@@ -184,6 +230,49 @@ __host__ size_t smem_bytes(int stages, int stage_bytes, size_t red_bytes)
 
 // ---------------------------------------------------------------- producer
 
+// Row -> window map for a producer's increasing rows.  The offsets of the
+// current segment stay in registers, so the next row of the same segment costs
+// no load; the binary search (dependent loads, slow under a full memory system)
+// runs once per segment change.  Same result as map_row.
+struct RowCursor {
+    int r0, r1;            // real rows: [cc[0], cc[n_seg])
+    int lo, hi, tok;       // current segment: rows [lo, hi), first token tok
+    int seg;
+};
+
+__device__ __forceinline__ void cursor_init(RowCursor &c, const int32_t *__restrict__ cc, int n_seg)
+{
+    c.r0 = n_seg > 0 ? __ldg(cc) : 0;
+    c.r1 = n_seg > 0 ? __ldg(cc + n_seg) : 0;
+    c.lo = c.hi = 0;
+    c.tok = 0;
+    c.seg = -1;
+}
+
+__device__ __forceinline__ RowMap cursor_map(RowCursor &c, int r, const int32_t *__restrict__ cu,
+                                             const int32_t *__restrict__ cc, int n_seg, int ratio)
+{
+    RowMap m;
+    m.base = 0;
+    m.seg = -1;
+    m.real = false;
+    m.first = true;
+    if (r < c.r0 || r >= c.r1)
+        return m;
+    if (c.seg < 0 || r < c.lo || r >= c.hi) {
+        c.seg = find_segment(cc, n_seg, r);
+        c.lo = __ldg(cc + c.seg);
+        c.hi = __ldg(cc + c.seg + 1);
+        c.tok = __ldg(cu + c.seg);
+    }
+    const int b = r - c.lo;
+    m.base = (int64_t)c.tok + (int64_t)b * ratio;
+    m.seg = c.seg;
+    m.real = true;
+    m.first = (b == 0);
+    return m;
+}
+
 // Issues the copies of rows row0, row0 + rstride, ... < rend.  Runs on one lane.
 template <int RATIO, int COFF, bool BWD>
 __device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int row0, int rstride, int rend,
@@ -193,10 +282,12 @@ __device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int 
     const uint32_t run = (uint32_t)tc * 2;
     int issued = 0, st = 0;
     uint32_t ph = 0;
+    RowCursor cur;
+    cursor_init(cur, a.cc, a.n_seg);
     for (int row = row0; row < rend; row += rstride) {
         if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
             break;
-        const RowMap rm = map_row(row, a.cu, a.cc, a.n_seg, RATIO);
+        const RowMap rm = cursor_map(cur, row, a.cu, a.cc, a.n_seg, RATIO);
         StageMeta &m = s.meta[st];
         m.base = rm.base;
         m.seg = rm.seg;
@@ -205,13 +296,20 @@ __device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int 
         m.first = rm.first;
         const bool load = BWD ? rm.real : true;
         const int p0 = (COFF == 2 && rm.first) ? 1 : 0;
-        const uint32_t bytes = load ? (uint32_t)((COFF - p0) * 2 * RATIO) * run + (BWD ? run : 0u) : 0u;
+        const uint32_t bytes =
+            load ? (uint32_t)((COFF - p0) * 2 * RATIO * a.rw * 2) + (BWD ? run : 0u) : 0u;
         const uint32_t fb = smem_addr(&s.full[st]);
         mbar_arrive_expect_tx(fb, bytes);
         if (load) {
             const uint32_t dst = smem_addr(s.stages + (size_t)st * a.stage_bytes);
             for (int p = p0; p < COFF; ++p) {
                 const int64_t tok0 = rm.base + (int64_t)(p - (COFF - 1)) * RATIO;
+                if (a.pcol) {
+                    const uint32_t blk = (uint32_t)(RATIO * C * 2);
+                    bulk_g2s(dst + stage_offset<RATIO, COFF>(0, p, 0, a.rw), a.kv + tok0 * C, blk, fb);
+                    bulk_g2s(dst + stage_offset<RATIO, COFF>(1, p, 0, a.rw), a.score + tok0 * C, blk, fb);
+                    continue;
+                }
                 const int64_t col = (int64_t)p * a.head_dim + c0;
 #pragma unroll
                 for (int i = 0; i < RATIO; ++i) {
@@ -221,7 +319,7 @@ __device__ void produce(const StreamArgs &a, const Smem &s, int tc, int c0, int 
                 }
             }
             if (BWD)
-                bulk_g2s(dst + window_bytes<RATIO, COFF>(tc), grad_out + (int64_t)row * a.head_dim + c0, run, fb);
+                bulk_g2s(dst + window_bytes<RATIO, COFF>(a.rw), grad_out + (int64_t)row * a.head_dim + c0, run, fb);
         }
         ++issued;
         if (++st == a.stages) {
@@ -256,15 +354,15 @@ __device__ __forceinline__ void load_ape(const StreamArgs &a, int col0, ApeRegs<
 
 // Reads the thread's kNP words (2*kNP bf16) of window position k from the stage.
 template <int RATIO, int COFF>
-__device__ __forceinline__ void stage_words(uint32_t (&w)[kNP], const unsigned char *stage, int arr, int k, int tc,
-                                            int lc)
+__device__ __forceinline__ void stage_words(uint32_t (&w)[kNP], const unsigned char *stage, int arr, int k, int rw,
+                                            int pcol, int lc)
 {
     const int p = k / RATIO, i = k % RATIO;
-    ld_np(w, stage + stage_offset<RATIO, COFF>(arr, p, i, tc) + lc * 2);
+    ld_np(w, stage + stage_offset<RATIO, COFF>(arr, p, i, rw) + (p * pcol + lc) * 2);
 }
 
 template <int RATIO, int COFF>
-__device__ __forceinline__ void pool_stage(const unsigned char *stage, int tc, int lc, bool first,
+__device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, int pcol, int lc, bool first,
                                            const ApeRegs<RATIO, COFF> &ap, uint32_t (&kvw)[COFF * RATIO][kNP],
                                            float2 (&e)[COFF * RATIO][kNP], float2 (&den)[kNP], float2 (&num)[kNP])
 {
@@ -278,8 +376,8 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int tc, i
         if (COFF == 2 && k < RATIO && first)
             continue;
         uint32_t sw[kNP];
-        stage_words<RATIO, COFF>(sw, stage, 1, k, tc, lc);
-        stage_words<RATIO, COFF>(kvw[k], stage, 0, k, tc, lc);
+        stage_words<RATIO, COFF>(sw, stage, 1, k, rw, pcol, lc);
+        stage_words<RATIO, COFF>(kvw[k], stage, 0, k, rw, pcol, lc);
 #pragma unroll
         for (int q = 0; q < kNP; ++q) {
             e[k][q] = add2(bf16x2_to_f2(sw[q]), ap.v[k][q]);
@@ -315,14 +413,15 @@ __global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG) fwd_stream_kernel(StreamArgs 
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int ncw = blockDim.x / 32 - 1;  // consumer warps; the last warp produces
-    const int tc = ncw * kColsPerWarp;
+    const int tc = a.tc;
     const int c0 = blockIdx.y * tc;
     const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const Lanes ln = lanes_of(a, warp, lane);
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(smem_addr(&s.full[i]), 1);
-            mbar_init(smem_addr(&s.empty[i]), ncw);
+            mbar_init(smem_addr(&s.empty[i]), ln.cols);
         }
         mbar_init_fence();
     }
@@ -334,19 +433,22 @@ __global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG) fwd_stream_kernel(StreamArgs 
             produce<RATIO, COFF, false>(a, s, tc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
         return;
     }
-    const int lc = threadIdx.x * kCPT;  // local column of this thread in the tile
+    const int lc = ln.lc;  // local column of this thread in the tile
     ApeRegs<RATIO, COFF> ap;
     load_ape<RATIO, COFF>(a, c0 + lc, ap);
-    int st = 0;
+    int st = ln.lane;
     uint32_t ph = 0;
-    for (int row = blockIdx.x; row < a.capacity; row += gridDim.x) {
+    for (int j = ln.lane;; j += a.row_lanes, ring_next(st, ph, a.row_lanes, a.stages)) {
+        const int row = blockIdx.x + j * gridDim.x;
+        if (row >= a.capacity)
+            break;
         if (!mbar_wait(smem_addr(&s.full[st]), ph, a.status))
             break;
         const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
         const bool first = s.meta[st].first;
         uint32_t kvw[COFF * RATIO][kNP];
         float2 e[COFF * RATIO][kNP], den[kNP], num[kNP];
-        pool_stage<RATIO, COFF>(stage, tc, lc, first, ap, kvw, e, den, num);
+        pool_stage<RATIO, COFF>(stage, a.rw, a.pcol, lc, first, ap, kvw, e, den, num);
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
@@ -355,10 +457,6 @@ __global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG) fwd_stream_kernel(StreamArgs 
         for (int q = 0; q < kNP; ++q)
             o[q] = f2_to_bf16x2(mul2(num[q], make_float2(recip_den(den[q].x), recip_den(den[q].y))));
         st_np(out + (int64_t)row * a.head_dim + c0 + lc, o);
-        if (++st == a.stages) {
-            st = 0;
-            ph ^= 1u;
-        }
     }
 }
 
@@ -399,15 +497,16 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
     constexpr int W = COFF * RATIO;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const int ncw = blockDim.x / 32 - 1;
-    const int tc = ncw * kColsPerWarp;
+    const int tc = a.tc;
     const int c0 = blockIdx.y * tc;
     const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const Lanes ln = lanes_of(a, warp, lane);
     const int64_t C = (int64_t)COFF * a.head_dim;
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(smem_addr(&s.full[i]), 1);
-            mbar_init(smem_addr(&s.empty[i]), ncw);
+            mbar_init(smem_addr(&s.empty[i]), ln.cols);
         }
         mbar_init_fence();
     }
@@ -425,14 +524,14 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
 #pragma unroll
         for (int q = 0; q < kNP; ++q)
             acc[k][q] = make_float2(0.0f, 0.0f);
-    const int lc = threadIdx.x * kCPT;
+    const int lc = ln.lc;
     const int col = c0 + lc;
 
     if (warp == ncw) {
         if (lane == 0)
             produce<RATIO, COFF, true>(a, s, tc, c0, blockIdx.x, gridDim.x, rend, grad_out);
     } else {
-        if (blockIdx.x == 0) {  // leading gap: tokens before the first real block
+        if (blockIdx.x == 0 && ln.lane == 0) {  // leading gap: tokens before the first real block
             int64_t lead = o.n_tokens;
             if (R0 < R)
                 lead = map_row(R0, a.cu, a.cc, a.n_seg, RATIO).base;
@@ -440,17 +539,14 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
         }
         ApeRegs<RATIO, COFF> ap;
         load_ape<RATIO, COFF>(a, col, ap);
-        int st = 0;
+        int st_used = ln.lane;
         uint32_t ph = 0;
-        for (int row = blockIdx.x; row < rend; row += gridDim.x) {
-            if (!mbar_wait(smem_addr(&s.full[st]), ph, a.status))
+        for (int j = ln.lane;; j += a.row_lanes, ring_next(st_used, ph, a.row_lanes, a.stages)) {
+            if (blockIdx.x + j * gridDim.x >= rend)
                 break;
-            const StageMeta m = s.meta[st];
-            const int st_used = st;
-            if (++st == a.stages) {
-                st = 0;
-                ph ^= 1u;
-            }
+            if (!mbar_wait(smem_addr(&s.full[st_used]), ph, a.status))
+                break;
+            const StageMeta m = s.meta[st_used];
             if (!m.real) {
                 __syncwarp();
                 if (lane == 0)
@@ -460,9 +556,9 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
             const unsigned char *stage = s.stages + (size_t)st_used * a.stage_bytes;
             uint32_t kvw[W][kNP];
             float2 e[W][kNP], den[kNP], num[kNP];
-            pool_stage<RATIO, COFF>(stage, tc, lc, m.first, ap, kvw, e, den, num);
+            pool_stage<RATIO, COFF>(stage, a.rw, a.pcol, lc, m.first, ap, kvw, e, den, num);
             uint32_t gw[kNP];
-            ld_np(gw, stage + window_bytes<RATIO, COFF>(tc) + lc * 2);
+            ld_np(gw, stage + window_bytes<RATIO, COFF>(a.rw) + lc * 2);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&s.empty[st_used]));
@@ -511,11 +607,12 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
                 zero_range<COFF>(o, C, a.head_dim, col, m.base + RATIO, next);
             }
         }
-        // this thread's grad_ape sums -> shared memory [ape row][part][tile column]
+        // this thread's grad_ape sums -> shared memory [row lane][ape row][part][tile column]
+        float *red = s.red + (size_t)ln.lane * RATIO * COFF * tc;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
             const int p = k / RATIO, i = k % RATIO;
-            st_pairs(s.red + (i * COFF + p) * tc + lc, acc[k]);
+            st_pairs(red + (i * COFF + p) * tc + lc, acc[k]);
         }
     }
     __syncthreads();
@@ -529,12 +626,16 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, int64_t n_
     const int i_lo = rank * share;
     const int i_hi = i_lo + share < n4 ? i_lo + share : n4;
     float *dst = partial + (int64_t)(blockIdx.x / nrank) * RATIO * C;
+    const int lane_floats = RATIO * COFF * tc;
     for (int i4 = i_lo + (int)threadIdx.x; i4 < i_hi; i4 += blockDim.x) {
         const int rp = (i4 * 4) / tc, lcol = i4 * 4 - rp * tc;
         const int arow = rp / COFF, p = rp - arow * COFF;
+        // ranks in ascending order, within a rank its row lanes in ascending order
         float4 acc4 = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(s.red, 0) + i4 * 4);
-        for (int q = 1; q < nrank; ++q) {
-            const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(s.red, q) + i4 * 4);
+        for (int t = 1; t < nrank * a.row_lanes; ++t) {
+            const int q = t / a.row_lanes, l = t - q * a.row_lanes;
+            const float4 v =
+                *reinterpret_cast<const float4 *>(cluster.map_shared_rank(s.red, q) + (size_t)l * lane_floats + i4 * 4);
             acc4.x = __fadd_rn(acc4.x, v.x);
             acc4.y = __fadd_rn(acc4.y, v.y);
             acc4.z = __fadd_rn(acc4.z, v.z);
@@ -566,13 +667,23 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     StreamPlan pl;
     pl.tc = tile_cols(head_dim);
     pl.tiles = head_dim / pl.tc;
-    pl.threads = (pl.tc / kColsPerWarp + 1) * 32;
-    const int win = 2 * coff * ratio * pl.tc * 2;
+    // Up to four consumer warps per block: tiles narrower than 512 columns take
+    // two rows at once (more would leave the block's one producer behind).
+    const int cols = pl.tc / kColsPerWarp;
+    pl.row_lanes = cols <= 2 ? 2 : 1;
+    const int warps = cols * pl.row_lanes;
+    pl.threads = (warps + 1) * 32;
+    // whole rows for one column tile of at most CSA_STREAM_WHOLE_MAX_D columns
+    pl.whole = pl.tiles == 1 && (coff == 1 || head_dim <= CSA_STREAM_WHOLE_MAX_D);
+    const int rw = pl.whole ? coff * head_dim : pl.tc;
+    const int win = 2 * coff * ratio * rw * 2;
     pl.stage_bytes = ((bwd ? win + pl.tc * 2 : win) + 127) / 128 * 128;
-    const int budget = bwd ? CSA_STREAM_BWD_BUDGET : CSA_STREAM_FWD_BUDGET;
-    pl.stages = budget / pl.stage_bytes;
-    pl.stages = pl.stages < 2 ? 2 : (pl.stages > 8 ? 8 : pl.stages);
-    pl.red_bytes = bwd ? (size_t)ratio * coff * pl.tc * sizeof(float) : 0;
+    // ring bytes in proportion to the consumer warps (the budget is for four)
+    const int budget = (bwd ? CSA_STREAM_BWD_BUDGET : CSA_STREAM_FWD_BUDGET) / 4 * warps;
+    int per_lane = budget / pl.stage_bytes / pl.row_lanes;
+    per_lane = per_lane < 2 ? 2 : (per_lane > 8 ? 8 : per_lane);
+    pl.stages = per_lane * pl.row_lanes;  // a multiple of the row lanes
+    pl.red_bytes = bwd ? (size_t)pl.row_lanes * ratio * coff * pl.tc * sizeof(float) : 0;
     pl.smem = smem_bytes(pl.stages, pl.stage_bytes, pl.red_bytes);
     pl.cluster = bwd ? CSA_STREAM_BWD_CLUSTER : 1;
     pl.num_sms = num_sms;
@@ -682,7 +793,7 @@ static cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl,
 {
     StreamArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
                  p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes,
-                 status};
+                 status, pl.tc, pl.row_lanes, pl.whole ? p.coff * p.head_dim : pl.tc, pl.whole ? p.head_dim : 0};
     int blocks = 0;
     cudaError_t e = blocks_for<RATIO, COFF>(pl, false, p.capacity, &blocks);
     if (e != cudaSuccess)
@@ -724,7 +835,7 @@ static cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl,
 {
     StreamArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
                  p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes,
-                 status};
+                 status, pl.tc, pl.row_lanes, pl.whole ? p.coff * p.head_dim : pl.tc, pl.whole ? p.head_dim : 0};
     int blocks = 0;
     cudaError_t e = blocks_for<RATIO, COFF>(pl, true, p.capacity, &blocks);
     if (e != cudaSuccess)

@@ -75,7 +75,8 @@ def test_tiny_bitwise(csa):
     assert np.abs(dape - d64).max() <= 1e-5 * np.abs(d64).max()
 
 
-@pytest.mark.parametrize("name", ["r4c2d512_8x4096", "r4c2d512_ragged64", "stress_unit", "stress_x64"])
+@pytest.mark.parametrize("name", ["r4c2d512_8x4096", "r4c2d512_ragged64", "stress_unit", "stress_x64",
+                                  "r4c2d128_32x4096", "r4c2d64_32x4096"])
 def test_workload_parity(csa, name):
     c = w.WORKLOADS[name]()
     check_against_oracle(c, csa, scale=64.0 if name == "stress_x64" else 1.0)
@@ -133,6 +134,27 @@ def test_small_layouts_bitwise(csa, coff, head_dim, li):
     d = Dev(c)
     if c.capacity > 0:
         assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))
+    dkv, dsc, dape = run_bwd(d, csa)
+    want = oracle.case_bwd_f32(c)
+    assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+    _, _, d64 = oracle.case_bwd_f64(c)
+    assert np.all(np.abs(dape - d64) <= 1e-5 * max(np.abs(d64).max(), 1e-30))
+
+
+@pytest.mark.parametrize("coff", [1, 2])
+@pytest.mark.parametrize("head_dim", [128, 256, 640])
+@pytest.mark.parametrize("li", [0, 2, 4, 6, 7, 9])
+def test_stream_row_lanes_bitwise(csa, coff, head_dim, li):
+    """Tiles of 128 and 256 columns (head_dim 128, 640: 128; 256: 256) run two
+    rows of a block side by side, and single-tile heads stage whole token rows;
+    any layout, any number of rows per block, gives the oracle's bits."""
+    lens = LAYOUTS[li] + [4 * 777 + 2]
+    extra = (0, 1, 5)[li % 3]
+    leading = (0, 3)[li % 2]
+    T = leading + sum(lens) + 2
+    c = w.make_case("lanes", 4, coff, head_dim, lens, extra_rows=extra, n_tokens=T, leading=leading, seed=li + 60)
+    d = Dev(c)
+    assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))
     dkv, dsc, dape = run_bwd(d, csa)
     want = oracle.case_bwd_f32(c)
     assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
