@@ -208,6 +208,9 @@ SPECS = {
     # head_dim 128 at ratio 128, coff 1, 4 x 131072 tokens
     "r128c1d128_4x131072": lambda seed=0: dict(name="r128c1d128_4x131072", ratio=128, coff=1, head_dim=128,
                                                seqlens=[131072] * 4),
+    # ratio 8 (generic kernels), coff 2, head_dim 512, 8 segments of 4096 tokens
+    "r8c2d512_8x4096": lambda seed=0: dict(name="r8c2d512_8x4096", ratio=8, coff=2, head_dim=512,
+                                           seqlens=[4096] * 8),
     # a ratio served by the generic kernels: ratio 16, coff 2, head_dim 512,
     # 8 segments of 4096 tokens (2048 rows), 64 padding rows
     "r16c2d512_8x4096": lambda seed=0: dict(name="r16c2d512_8x4096", ratio=16, coff=2, head_dim=512,

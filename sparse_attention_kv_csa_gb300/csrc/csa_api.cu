@@ -6,6 +6,9 @@
 // (ratio, head_dim), int32 flat offsets, total_comp > 0 requiring at least ratio
 // tokens, 16-byte aligned tensor bases (4-byte for the int32 offsets) checked per
 // call.  Nothing is launched and no output is touched when validation fails.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -180,6 +183,130 @@ cudaError_t allow_max_smem(const void *fn)
     return e;
 }
 
+// Resident blocks of a kernel configuration, computed once per (device, kernel,
+// block size, shared memory, cluster) and cached: the occupancy queries and the
+// shared-memory attribute are host calls too slow to repeat on every launch.
+namespace {
+
+struct ResidentKey {
+    int dev;
+    const void *fn;
+    int threads;
+    size_t smem;
+    int cluster;
+};
+
+cudaError_t cached_resident(const ResidentKey &k, int *resident, cudaError_t (*query)(const ResidentKey &, int *))
+{
+    static std::mutex mu;
+    static ResidentKey keys[64];
+    static int vals[64];
+    static int n = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (int i = 0; i < n; ++i)
+            if (keys[i].dev == k.dev && keys[i].fn == k.fn && keys[i].threads == k.threads &&
+                keys[i].smem == k.smem && keys[i].cluster == k.cluster) {
+                *resident = vals[i];
+                return cudaSuccess;
+            }
+    }
+    cudaError_t e = query(k, resident);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> g(mu);
+    if (n < 64) {
+        keys[n] = k;
+        vals[n] = *resident;
+        ++n;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t query_resident(const ResidentKey &k, int *resident)
+{
+    // The kernel's dynamic shared-memory limit is a per-function attribute shared by
+    // every configuration: raise it to the device maximum (not to this plan's size,
+    // which a later plan of another head_dim could undercut).
+    cudaError_t e = allow_max_smem(k.fn);
+    if (e != cudaSuccess)
+        return e;
+    if (k.cluster > 1) {
+        // clusters are placed within GPCs: ask how many fit, not blocks per SM
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(k.cluster, 1, 1);
+        cfg.blockDim = dim3(k.threads, 1, 1);
+        cfg.dynamicSmemBytes = k.smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = k.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, k.fn, &cfg);
+        *resident = clusters * k.cluster;
+        return e;
+    }
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, k.threads, k.smem);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, k.dev);
+    *resident = per_sm * sms;
+    return e;
+}
+
+}  // namespace
+
+cudaError_t resident_blocks(const void *fn, int threads, size_t smem, int cluster, int *resident)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    return cached_resident(ResidentKey{dev, fn, threads, smem, cluster}, resident, query_resident);
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t *err)
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static cudaError_t e = cudaSuccess;
+    std::call_once(once, []() {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+        if (e == cudaSuccess && q != cudaDriverEntryPointSuccess)
+            e = cudaErrorNotSupported;
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    *err = e;
+    return fn;
+}
+
+}  // namespace
+
+// The row extent is the int32 flat-offset bound, not the (unknown to the forward)
+// token count: every box the kernels request lies inside a real block.
+cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int box_cols, int box_rows)
+{
+    cudaError_t e;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn(&e);
+    if (e != cudaSuccess)
+        return e;
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(((int64_t)1 << 31) / C)};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int fail_status(int status, const char *fmt, ...)
 {
     va_list ap;
@@ -241,7 +368,7 @@ int csa_compress_fwd(const void *kv, const void *score, const float *ape, const 
     if (csa::r128_supported(ratio, coff, head_dim))
         e = csa::launch_fwd_r128(p, ds->status, st);
     else if (ratio != 4)
-        e = csa::launch_fwd_generic(p, ds->num_sms, st);
+        e = csa::launch_fwd_generic(p, ds->status, ds->num_sms, st);
     else if (csa::stream_supported(ratio, coff, head_dim))
         e = csa::launch_fwd_stream(p, csa::plan_stream(false, ratio, coff, head_dim, capacity, ds->num_sms),
                                    ds->status, st);
@@ -295,7 +422,9 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
             return cuda_fail(e, "backward plan");
         floats = (int64_t)partials * ratio * coff * head_dim;
     } else if (generic) {
-        gp = csa::plan_generic(ratio, coff, head_dim, capacity, ds->num_sms);
+        e = csa::plan_generic(ratio, coff, head_dim, capacity, ds->num_sms, &gp);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "backward plan");
         floats = gp.partial_floats;
     } else if (streamed) {
         sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, ds->num_sms);
@@ -311,7 +440,7 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
     if (r128)
         e = csa::launch_bwd_r128(p, static_cast<float *>(partial), r128_blocks, ds->status, st);
     else if (generic)
-        e = csa::launch_bwd_generic(p, gp, static_cast<float *>(partial), st);
+        e = csa::launch_bwd_generic(p, gp, static_cast<float *>(partial), ds->status, st);
     else if (streamed)
         e = csa::launch_bwd_stream(p, sp, static_cast<float *>(partial), ds->status, st);
     else

@@ -163,6 +163,49 @@ __device__ __forceinline__ RowMap map_row(int r, const int32_t *__restrict__ cu,
     return m;
 }
 
+// Row -> window map for one thread's increasing rows.  The offsets of the
+// current segment stay in registers, so the next row of the same segment costs
+// no load; the binary search (dependent loads, slow under a full memory system)
+// runs once per segment change.  Same result as map_row.
+struct RowCursor {
+    int r0, r1;            // real rows: [cc[0], cc[n_seg])
+    int lo, hi, tok;       // current segment: rows [lo, hi), first token tok
+    int seg;
+};
+
+__device__ __forceinline__ void cursor_init(RowCursor &c, const int32_t *__restrict__ cc, int n_seg)
+{
+    c.r0 = n_seg > 0 ? __ldg(cc) : 0;
+    c.r1 = n_seg > 0 ? __ldg(cc + n_seg) : 0;
+    c.lo = c.hi = 0;
+    c.tok = 0;
+    c.seg = -1;
+}
+
+__device__ __forceinline__ RowMap cursor_map(RowCursor &c, int r, const int32_t *__restrict__ cu,
+                                             const int32_t *__restrict__ cc, int n_seg, int ratio)
+{
+    RowMap m;
+    m.base = 0;
+    m.seg = -1;
+    m.real = false;
+    m.first = true;
+    if (r < c.r0 || r >= c.r1)
+        return m;
+    if (c.seg < 0 || r < c.lo || r >= c.hi) {
+        c.seg = find_segment(cc, n_seg, r);
+        c.lo = __ldg(cc + c.seg);
+        c.hi = __ldg(cc + c.seg + 1);
+        c.tok = __ldg(cu + c.seg);
+    }
+    const int b = r - c.lo;
+    m.base = (int64_t)c.tok + (int64_t)b * ratio;
+    m.seg = c.seg;
+    m.real = true;
+    m.first = (b == 0);
+    return m;
+}
+
 // 16-byte streaming load (read once: evict-first in L1 and L2).
 __device__ __forceinline__ uint4 ld_stream(const void *p) { return __ldcs(reinterpret_cast<const uint4 *>(p)); }
 
@@ -252,6 +295,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     }
     atomicCAS(status, 0u, kStatusTimeout);
     return false;
+}
+
+// Next slot of a row lane: `step` slots on, the phase flipping on each wrap
+// (stages is a multiple of step).
+__device__ __forceinline__ void ring_next(int &st, uint32_t &ph, int step, int stages)
+{
+    st += step;
+    if (st >= stages) {
+        st -= stages;
+        ph ^= 1u;
+    }
 }
 
 // Contiguous global -> shared copy of `bytes` (16-byte aligned ends), completing

@@ -1,8 +1,10 @@
 // Compressor kernels for every other ratio: 1 <= ratio <= 128, windows of up to
 // 256 positions ("CSA Fused Compressor", cuDNN frontend docs, section Semantics;
-// the page's generic kernels are generic over the ratio as well).
+// the page's generic kernels are generic over the ratio as well).  Two families:
+// the staged kernels (further down) for windows of at most 64 positions on
+// head_dim a multiple of 64, and the global-memory walk below for the rest.
 //
-// One thread owns four adjacent columns j .. j+3 (two fp32 pairs) of one output
+// Global-memory walk: one thread owns four adjacent columns j .. j+3 (two fp32 pairs) of one output
 // row and walks the window three times (max; exp and sums; gradients), straight
 // from global memory: the window is too long for registers at large ratios and
 // the re-reads of a row's window hit L1/L2, so DRAM traffic stays the algorithmic
@@ -322,6 +324,438 @@ __global__ void __launch_bounds__(kGenBwdGroups * kGenBwdMaxLanes, 2)
     }
 }
 
+
+// ------------------------------------------------------------ staged kernels
+// Windows of at most kGsMaxWindow positions on head_dim a multiple of 64: the
+// window is staged through shared memory instead of walked in global memory.  A
+// block owns a 64-column tile; one producer thread streams its rows' windows with
+// 2-D TMA boxes (per part and array one [ratio x 64] box) into a ring of stages;
+// each consumer warp takes whole rows (row lane l: the block's rows l, l + lanes,
+// ...), a row's 64 columns at two per thread, and walks the window in shared
+// memory: max, then exp / sums, then (backward) the gradients, with the tile's
+// APE rows held in shared memory for the whole block.  Narrow tiles keep a row's
+// stage small, so many rows (warps) are in flight per SM.  Same arithmetic and
+// order as the rest of the library.  Backward grad_ape: each thread sums its
+// rows' ds per window position in its own shared-memory slots; lanes are added
+// in ascending order and the block writes one partial [ratio, C] for its columns.
+
+constexpr int kGsTile = 64;       // columns per block tile (two per consumer thread)
+constexpr int kGsMaxWindow = 64;  // coff * ratio
+constexpr int kGsMaxLanes = 4;    // consumer warps per block
+#ifndef CSA_GS_BUDGET
+#define CSA_GS_BUDGET (64 * 1024)
+#endif
+constexpr int kGsRingBudget = CSA_GS_BUDGET;
+constexpr size_t kGsSmemPerSM = 228 * 1024;  // shared memory per SM, 1 KB of it reserved per block
+
+struct GsArgs {
+    GenArgs g;
+    int stages;       // ring depth, a multiple of the consumer warps
+    int stage_bytes;  // window (+ grad_out row), a multiple of 128
+    unsigned *status;
+};
+
+struct GsMeta {
+    int64_t base;
+    int seg;
+    int row;
+    int real;
+    int first;
+    int pad[2];
+};
+
+struct GsSmem {
+    unsigned char *stages;  // [stage][array][part][ratio][kGsTile] bf16 (+ grad_out row)
+    GsMeta *meta;
+    uint64_t *full;
+    uint64_t *empty;
+    float *apet;  // [window position][kGsTile]
+    float2 *acc;  // backward: [lane][window position][32 threads]
+};
+
+size_t gs_smem_bytes(int stages, int stage_bytes, int W, int lanes, bool bwd)
+{
+    return 128 + (size_t)stages * stage_bytes + (sizeof(GsMeta) + 16) * stages + (size_t)W * kGsTile * sizeof(float) +
+           (bwd ? (size_t)lanes * W * 32 * sizeof(float2) : 0);
+}
+
+__device__ __forceinline__ GsSmem gs_carve(unsigned char *raw, int stages, int stage_bytes, int W)
+{
+    GsSmem s;
+    unsigned char *p = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127));
+    s.stages = p;
+    p += (size_t)stages * stage_bytes;
+    s.meta = reinterpret_cast<GsMeta *>(p);
+    p += sizeof(GsMeta) * stages;
+    s.full = reinterpret_cast<uint64_t *>(p);
+    s.empty = s.full + stages;
+    p = reinterpret_cast<unsigned char *>(s.empty + stages);
+    s.apet = reinterpret_cast<float *>(p);
+    p += (size_t)W * kGsTile * sizeof(float);
+    s.acc = reinterpret_cast<float2 *>(p);
+    return s;
+}
+
+// Issues the window copies of rows row0, row0 + rstride, ... < rend.  One thread.
+template <bool BWD>
+__device__ void gs_produce(const GsArgs &a, const GsSmem &s, const CUtensorMap *tm_kv, const CUtensorMap *tm_sc,
+                           int c0, int row0, int rstride, int rend, const uint16_t *__restrict__ grad_out)
+{
+    const GenArgs &g = a.g;
+    const uint32_t part_bytes = (uint32_t)g.ratio * kGsTile * 2;
+    int issued = 0, st = 0;
+    uint32_t ph = 0;
+    RowCursor cur;
+    cursor_init(cur, g.cc, g.n_seg);
+    for (int row = row0; row < rend; row += rstride) {
+        if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
+            break;
+        const RowMap rm = cursor_map(cur, row, g.cu, g.cc, g.n_seg, g.ratio);
+        GsMeta &m = s.meta[st];
+        m.base = rm.base;
+        m.seg = rm.seg;
+        m.row = row;
+        m.real = rm.real;
+        m.first = rm.first;
+        const bool load = BWD ? rm.real : true;
+        const int p0 = (g.coff == 2 && rm.first) ? 1 : 0;
+        const uint32_t bytes = load ? (uint32_t)(g.coff - p0) * 2u * part_bytes + (BWD ? kGsTile * 2u : 0u) : 0u;
+        const uint32_t fb = smem_addr(&s.full[st]);
+        mbar_arrive_expect_tx(fb, bytes);
+        if (load) {
+            const uint32_t dst = smem_addr(s.stages + (size_t)st * a.stage_bytes);
+            for (int p = p0; p < g.coff; ++p) {
+                const int y = (int)(rm.base + (int64_t)(p - (g.coff - 1)) * g.ratio);
+                const int x = p * g.head_dim + c0;
+                tma_load_2d(dst + (uint32_t)p * part_bytes, tm_kv, x, y, fb);
+                tma_load_2d(dst + (uint32_t)(g.coff + p) * part_bytes, tm_sc, x, y, fb);
+            }
+            if (BWD)
+                bulk_g2s(dst + 2u * g.coff * part_bytes, grad_out + (int64_t)row * g.head_dim + c0, kGsTile * 2, fb);
+        }
+        ++issued;
+        if (++st == a.stages) {
+            st = 0;
+            ph ^= 1u;
+        }
+    }
+    const int lo = issued > a.stages ? issued - a.stages : 0;
+    for (int it = lo; it < issued; ++it)
+        mbar_wait(smem_addr(&s.full[it % a.stages]), (uint32_t)(it / a.stages) & 1u, a.status);
+}
+
+// The tile's APE rows, [window position k][tile column], by the consumer threads.
+__device__ __forceinline__ void gs_load_ape(const GenArgs &g, float *apet, int c0, int t, int nthreads)
+{
+    const int W = g.coff * g.ratio;
+    const int64_t C = (int64_t)g.coff * g.head_dim;
+    for (int idx = t; idx < W * (kGsTile / 4); idx += nthreads) {
+        const int k = idx / (kGsTile / 4), c4 = idx % (kGsTile / 4);
+        const int p = k / g.ratio, i = k % g.ratio;
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(g.ape + i * C + (int64_t)p * g.head_dim + c0 + 4 * c4));
+        *reinterpret_cast<float4 *>(apet + k * kGsTile + 4 * c4) = v;
+    }
+}
+
+// Logits of window position k for the thread's two columns (stage + APE tile).
+__device__ __forceinline__ float2 gs_logits(const unsigned char *sc, const float *ap, int k)
+{
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(sc + k * (kGsTile * 2));
+    return add2(bf16x2_to_f2(w), *reinterpret_cast<const float2 *>(ap + k * kGsTile));
+}
+
+// Passes 1 and 2 over the staged window (positions k0 .. W-1 of at most WMAX):
+// the logits, then e = EXP(s - m) in place, in registers (the window loop is
+// unrolled to WMAX, positions outside [k0, W) skipped); m, den, num.
+template <int WMAX>
+__device__ __forceinline__ void gs_pool(const unsigned char *kvp, const unsigned char *sc, const float *ap, int k0,
+                                        int W, float2 (&e)[WMAX], float2 &m, float2 &den, float2 &num)
+{
+    m = make_float2(-INFINITY, -INFINITY);
+#pragma unroll
+    for (int k = 0; k < WMAX; ++k)
+        if (k >= k0 && k < W) {
+            e[k] = gs_logits(sc, ap, k);
+            m.x = max_nan(m.x, e[k].x);
+            m.y = max_nan(m.y, e[k].y);
+        }
+    const float2 negm = make_float2(-m.x, -m.y);
+    den = num = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < WMAX; ++k)
+        if (k >= k0 && k < W) {
+            e[k] = exp2lanes(add2(e[k], negm));
+            den = add2(den, e[k]);
+            num = fma2(e[k], bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(kvp + k * (kGsTile * 2))), num);
+        }
+}
+
+template <int WMAX>
+__global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
+    fwd_gs_kernel(GsArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                  uint16_t *__restrict__ out)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const GenArgs &g = a.g;
+    const int W = g.coff * g.ratio;
+    const int lanes = blockDim.x / 32 - 1;
+    const int c0 = blockIdx.y * kGsTile;
+    const GsSmem s = gs_carve(smem_raw, a.stages, a.stage_bytes, W);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(smem_addr(&s.full[i]), 1);
+            mbar_init(smem_addr(&s.empty[i]), 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    if (warp == lanes) {
+        if (lane == 0)
+            gs_produce<false>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, g.capacity, nullptr);
+        return;
+    }
+    gs_load_ape(g, s.apet, c0, threadIdx.x, lanes * 32);
+    named_barrier(1, lanes * 32);
+    const int lc = lane * 2;
+    const size_t sc_off = (size_t)g.coff * g.ratio * kGsTile * 2;
+    int st = warp;
+    uint32_t ph = 0;
+    for (int j = warp;; j += lanes, ring_next(st, ph, lanes, a.stages)) {
+        const int row = blockIdx.x + j * gridDim.x;
+        if (row >= g.capacity)
+            break;
+        if (!mbar_wait(smem_addr(&s.full[st]), ph, a.status))
+            break;
+        const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes + lc * 2;
+        const int k0 = (g.coff == 2 && s.meta[st].first) ? g.ratio : 0;
+        float2 e[WMAX], m, den, num;
+        gs_pool<WMAX>(stage, stage + sc_off, s.apet + lc, k0, W, e, m, den, num);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_addr(&s.empty[st]));
+        const uint32_t o = f2_to_bf16x2(mul2(num, make_float2(recip_den(den.x), recip_den(den.y))));
+        *reinterpret_cast<uint32_t *>(out + (int64_t)row * g.head_dim + c0 + lc) = o;
+    }
+}
+
+// Zero the gradient slots of tokens [t0, t1) in the thread's two columns j, j+1
+// (first half only, or every half).
+__device__ __forceinline__ void gs_zero(const GenArgs &a, uint16_t *dkv, uint16_t *dscore, int64_t C, int j,
+                                        int64_t t0, int64_t t1, int64_t n_tokens, bool all_halves)
+{
+    t1 = t1 < n_tokens ? t1 : n_tokens;
+    for (int64_t t = t0 < 0 ? 0 : t0; t < t1; ++t) {
+        *reinterpret_cast<uint32_t *>(dkv + t * C + j) = 0u;
+        *reinterpret_cast<uint32_t *>(dscore + t * C + j) = 0u;
+        if (a.coff == 2 && all_halves) {
+            *reinterpret_cast<uint32_t *>(dkv + t * C + a.head_dim + j) = 0u;
+            *reinterpret_cast<uint32_t *>(dscore + t * C + a.head_dim + j) = 0u;
+        }
+    }
+}
+
+template <int WMAX>
+__global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
+    bwd_gs_kernel(GsArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                  int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
+                  uint16_t *__restrict__ dscore, float *__restrict__ partial)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    const GenArgs &g = a.g;
+    const int W = g.coff * g.ratio;
+    const int lanes = blockDim.x / 32 - 1;
+    const int c0 = blockIdx.y * kGsTile;
+    const GsSmem s = gs_carve(smem_raw, a.stages, a.stage_bytes, W);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t C = (int64_t)g.coff * g.head_dim;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(smem_addr(&s.full[i]), 1);
+            mbar_init(smem_addr(&s.empty[i]), 1);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();  // the grad_ape finalisation may launch; it waits for this grid's end
+    const int R = g.n_seg > 0 ? __ldg(g.cc + g.n_seg) : 0;
+    const int R0 = g.n_seg > 0 ? __ldg(g.cc) : 0;
+    const int rend = R < g.capacity ? R : g.capacity;  // padding rows carry no gradient
+    const int64_t n_tokens = n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(g.cu + g.n_seg);
+    const int lc = lane * 2;
+    const int j0 = c0 + lc;  // the thread's first-half column
+
+    if (warp == lanes) {
+        if (lane == 0)
+            gs_produce<true>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, rend, grad_out);
+    } else {
+        gs_load_ape(g, s.apet, c0, threadIdx.x, lanes * 32);
+        float2 *mine = s.acc + (size_t)warp * W * 32 + lane;  // slot k at mine[k * 32]
+        for (int k = 0; k < W; ++k)
+            mine[k * 32] = make_float2(0.0f, 0.0f);
+        named_barrier(1, lanes * 32);
+        if (blockIdx.x == 0 && warp == 0) {  // leading gap: tokens before the first real block
+            int64_t lead = n_tokens;
+            if (R0 < R)
+                lead = map_row(R0, g.cu, g.cc, g.n_seg, g.ratio).base;
+            gs_zero(g, dkv, dscore, C, j0, 0, lead, n_tokens, true);
+        }
+        const size_t sc_off = (size_t)g.coff * g.ratio * kGsTile * 2;
+        const size_t go_off = 2 * sc_off;
+        int st = warp;
+        uint32_t ph = 0;
+        for (int j = warp;; j += lanes, ring_next(st, ph, lanes, a.stages)) {
+            if (blockIdx.x + j * gridDim.x >= rend)
+                break;
+            if (!mbar_wait(smem_addr(&s.full[st]), ph, a.status))
+                break;
+            const GsMeta m = s.meta[st];
+            if (!m.real) {
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(&s.empty[st]));
+                continue;
+            }
+            const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
+            const unsigned char *kvp = stage + lc * 2, *sc = stage + sc_off + lc * 2;
+            const float *ap = s.apet + lc;
+            const int k0 = (g.coff == 2 && m.first) ? g.ratio : 0;
+            float2 e[WMAX], mx, den, num;
+            gs_pool<WMAX>(kvp, sc, ap, k0, W, e, mx, den, num);
+            const float2 gg = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(stage + go_off + lc * 2));
+            const float2 inv = make_float2(recip_den(den.x), recip_den(den.y));
+            const float2 go = mul2(gg, mul2(num, inv));
+            const float2 ngo = make_float2(-go.x, -go.y);
+            // window position k reads token tok_k = base - (coff-1)*ratio + k at packed
+            // column p*head_dim + j0, p = 1 for the own block's half (coff 2, k >= ratio)
+            const int64_t tok_k0 = m.base - (int64_t)(g.coff - 1) * g.ratio;
+            const int64_t lim = n_tokens - tok_k0;  // positions k < lim have a token
+            // gradient slot of position k: token row tok_k0 + k, the part's column;
+            // walked by one offset stepped per position (nothing hoisted per k)
+            int64_t o = (tok_k0 + k0) * C + j0 + ((g.coff == 2 && k0 >= g.ratio) ? g.head_dim : 0);
+#pragma unroll
+            for (int k = 0; k < WMAX; ++k)
+                if (k >= k0 && k < W) {
+                    if (g.coff == 2 && k == g.ratio && k0 == 0)
+                        o += g.head_dim;  // into the own block's half
+                    const float2 pk = mul2(e[k], inv);
+                    const float2 kvf = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(kvp + k * (kGsTile * 2)));
+                    const float2 ds = mul2(pk, add2(mul2(gg, kvf), ngo));
+                    mine[k * 32] = add2(mine[k * 32], ds);
+                    if (k < lim) {
+                        *reinterpret_cast<uint32_t *>(dkv + o) = f2_to_bf16x2(mul2(gg, pk));
+                        *reinterpret_cast<uint32_t *>(dscore + o) = f2_to_bf16x2(ds);
+                    }
+                    o += C;
+                }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(&s.empty[st]));
+            if (m.row + 1 == __ldg(g.cc + m.seg + 1)) {  // last block of its segment
+                if (g.coff == 2)  // own block's first-half columns: read by no row
+                    gs_zero(g, dkv, dscore, C, j0, m.base, m.base + g.ratio, n_tokens, false);
+                int64_t next = n_tokens;
+                if (m.row + 1 < R)
+                    next = map_row(m.row + 1, g.cu, g.cc, g.n_seg, g.ratio).base;
+                gs_zero(g, dkv, dscore, C, j0, m.base + g.ratio, next, n_tokens, true);
+            }
+        }
+    }
+    __syncthreads();
+    // lanes added in ascending order; the block's partial [ape row][packed column]
+    float *dst = partial + (int64_t)blockIdx.x * g.ratio * C;
+    for (int idx = threadIdx.x; idx < W * 32; idx += blockDim.x) {
+        const int k = idx / 32, t = idx % 32;
+        float2 sum = s.acc[(size_t)k * 32 + t];
+        for (int l = 1; l < lanes; ++l) {
+            const float2 v = s.acc[((size_t)l * W + k) * 32 + t];
+            sum.x = __fadd_rn(sum.x, v.x);
+            sum.y = __fadd_rn(sum.y, v.y);
+        }
+        const int p = k / g.ratio, i = k % g.ratio;
+        *reinterpret_cast<float2 *>(dst + (int64_t)i * C + (int64_t)p * g.head_dim + c0 + 2 * t) = sum;
+    }
+}
+
+struct GsPlan {
+    int wmax;  // register window bucket: 8, 16, 32 or 64 >= coff * ratio
+    int lanes;
+    int stages;
+    int stage_bytes;
+    int threads;
+    int tiles;
+    size_t smem;
+};
+
+bool gs_supported(int ratio, int coff, int head_dim)
+{
+    return head_dim % kGsTile == 0 && coff * ratio <= kGsMaxWindow && ratio >= 1;
+}
+
+// Consumer warps per block (1, 2 or 4, each with at least two stages of its own)
+// chosen for the most rows in flight per SM by shared memory.
+GsPlan gs_plan(bool bwd, int ratio, int coff, int head_dim)
+{
+    GsPlan best{};
+    const int W = coff * ratio;
+    const int wmax = W <= 8 ? 8 : W <= 16 ? 16 : W <= 32 ? 32 : 64;
+    const int stage_bytes = (2 * W * kGsTile * 2 + (bwd ? kGsTile * 2 : 0) + 127) / 128 * 128;
+    int best_warps = -1;
+    for (int lanes = kGsMaxLanes; lanes >= 1; lanes /= 2) {
+        GsPlan pl;
+        pl.wmax = wmax;
+        pl.lanes = lanes;
+        pl.stage_bytes = stage_bytes;
+        pl.tiles = head_dim / kGsTile;
+        int per_lane = kGsRingBudget / stage_bytes / lanes;
+        per_lane = per_lane < 2 ? 2 : (per_lane > 8 ? 8 : per_lane);
+        pl.stages = per_lane * lanes;
+        pl.smem = gs_smem_bytes(pl.stages, stage_bytes, W, lanes, bwd);
+        pl.threads = (lanes + 1) * 32;
+        const int per_sm = (int)(kGsSmemPerSM / (pl.smem + 1024));
+        const int warps = (per_sm > 16 ? 16 : per_sm) * lanes;
+        if (warps > best_warps) {
+            best_warps = warps;
+            best = pl;
+        }
+    }
+    return best;
+}
+
+template <int WMAX>
+const void *gs_fn(bool bwd)
+{
+    return bwd ? reinterpret_cast<const void *>(bwd_gs_kernel<WMAX>) : reinterpret_cast<const void *>(fwd_gs_kernel<WMAX>);
+}
+
+const void *gs_kernel(bool bwd, int wmax)
+{
+    switch (wmax) {
+    case 8: return gs_fn<8>(bwd);
+    case 16: return gs_fn<16>(bwd);
+    case 32: return gs_fn<32>(bwd);
+    default: return gs_fn<64>(bwd);
+    }
+}
+
+// Grid width (row blocks per column tile) of a staged launch.
+cudaError_t gs_blocks(bool bwd, const GsPlan &pl, int capacity, int *blocks)
+{
+    const void *fn = gs_kernel(bwd, pl.wmax);
+    int resident = 0;
+    cudaError_t e = resident_blocks(fn, pl.threads, pl.smem, 1, &resident);
+    if (e != cudaSuccess)
+        return e;
+    int b = (resident > 0 ? resident : 1) / pl.tiles;
+    b = b < 1 ? 1 : b;
+    const int rows = capacity > 0 ? capacity : 1;
+    *blocks = b < rows ? b : rows;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 bool generic_supported(int ratio, int coff, int head_dim)
@@ -329,7 +763,7 @@ bool generic_supported(int ratio, int coff, int head_dim)
     return ratio >= 1 && ratio <= 128 && (coff == 1 || coff == 2) && head_dim % 8 == 0 && head_dim <= 8192;
 }
 
-GenericPlan plan_generic(int ratio, int coff, int head_dim, int capacity, int num_sms)
+cudaError_t plan_generic(int ratio, int coff, int head_dim, int capacity, int num_sms, GenericPlan *out)
 {
     GenericPlan pl;
     const int groups4 = head_dim / 4;
@@ -350,51 +784,101 @@ GenericPlan plan_generic(int ratio, int coff, int head_dim, int capacity, int nu
     pl.smem = lane_bytes * pl.lanes;
     pl.partial_floats = (int64_t)pl.groups * ratio * coff * head_dim;
     pl.num_sms = num_sms;
-    return pl;
+    pl.staged_blocks = 0;
+    if (gs_supported(ratio, coff, head_dim)) {  // one partial per row block of the staged kernel
+        cudaError_t e = gs_blocks(true, gs_plan(true, ratio, coff, head_dim), capacity, &pl.staged_blocks);
+        if (e != cudaSuccess)
+            return e;
+        pl.partial_floats = (int64_t)pl.staged_blocks * ratio * coff * head_dim;
+    }
+    *out = pl;
+    return cudaSuccess;
 }
 
-cudaError_t launch_fwd_generic(const FwdParams &p, int num_sms, cudaStream_t st)
+cudaError_t launch_fwd_generic(const FwdParams &p, unsigned *status, int num_sms, cudaStream_t st)
 {
     GenArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
               p.cu_seqlens_comp, p.n_seg, p.ratio, p.coff, p.head_dim, p.capacity};
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (gs_supported(p.ratio, p.coff, p.head_dim)) {
+        const GsPlan pl = gs_plan(false, p.ratio, p.coff, p.head_dim);
+        int blocks = 0;
+        cudaError_t e = gs_blocks(false, pl, p.capacity, &blocks);
+        if (e != cudaSuccess)
+            return e;
+        CUtensorMap mk, ms;
+        const int64_t C = (int64_t)p.coff * p.head_dim;
+        if ((e = make_tensor_map_2d(&mk, p.kv, C, kGsTile, p.ratio)) != cudaSuccess ||
+            (e = make_tensor_map_2d(&ms, p.score, C, kGsTile, p.ratio)) != cudaSuccess)
+            return e;
+        GsArgs ga{a, pl.stages, pl.stage_bytes, status};
+        uint16_t *o = static_cast<uint16_t *>(p.out);
+        void *args[] = {&ga, &mk, &ms, &o};
+        cfg.gridDim = dim3(blocks, pl.tiles, 1);
+        cfg.blockDim = dim3(pl.threads, 1, 1);
+        cfg.dynamicSmemBytes = pl.smem;
+        return cudaLaunchKernelExC(&cfg, gs_kernel(false, pl.wmax), args);
+    }
     const int64_t units = (int64_t)p.capacity * (p.head_dim / 4);
     int64_t grid = (units + kGenFwdThreads - 1) / kGenFwdThreads;
     const int64_t cap = 8 * (int64_t)num_sms;
     grid = grid < cap ? grid : cap;
     grid = grid < 1 ? 1 : grid;
-    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(kGenFwdThreads, 1, 1);
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1] = {pdl_attribute()};
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fwd_generic_kernel, a, static_cast<uint16_t *>(p.out));
 }
 
-cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float *partial, cudaStream_t st)
+cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float *partial, unsigned *status,
+                               cudaStream_t st)
 {
     GenArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
               p.cu_seqlens_comp, p.n_seg, p.ratio, p.coff, p.head_dim, p.capacity};
-    if (pl.smem > 48 * 1024) {
-        cudaError_t e = allow_max_smem(reinterpret_cast<const void *>(bwd_generic_kernel));
-        if (e != cudaSuccess)
-            return e;
-    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.groups, pl.col_tiles, 1);
-    cfg.blockDim = dim3(kGenBwdGroups, pl.lanes, 1);
-    cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_generic_kernel, a, pl.rows_per_group, p.n_tokens,
-                                       static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
-                                       static_cast<uint16_t *>(p.dscore), partial);
+    cudaError_t e;
+    int n_partials = pl.groups;
+    if (pl.staged_blocks > 0) {
+        const GsPlan gp = gs_plan(true, p.ratio, p.coff, p.head_dim);
+        CUtensorMap mk, ms;
+        const int64_t C = (int64_t)p.coff * p.head_dim;
+        if ((e = allow_max_smem(gs_kernel(true, gp.wmax))) != cudaSuccess ||
+            (e = make_tensor_map_2d(&mk, p.kv, C, kGsTile, p.ratio)) != cudaSuccess ||
+            (e = make_tensor_map_2d(&ms, p.score, C, kGsTile, p.ratio)) != cudaSuccess)
+            return e;
+        GsArgs ga{a, gp.stages, gp.stage_bytes, status};
+        int64_t n_tokens = p.n_tokens;
+        const uint16_t *go = static_cast<const uint16_t *>(p.grad_out);
+        uint16_t *dk = static_cast<uint16_t *>(p.dkv), *dsc = static_cast<uint16_t *>(p.dscore);
+        void *args[] = {&ga, &mk, &ms, &n_tokens, &go, &dk, &dsc, &partial};
+        cfg.gridDim = dim3(pl.staged_blocks, gp.tiles, 1);
+        cfg.blockDim = dim3(gp.threads, 1, 1);
+        cfg.dynamicSmemBytes = gp.smem;
+        e = cudaLaunchKernelExC(&cfg, gs_kernel(true, gp.wmax), args);
+        n_partials = pl.staged_blocks;
+    } else {
+        if (pl.smem > 48 * 1024) {
+            e = allow_max_smem(reinterpret_cast<const void *>(bwd_generic_kernel));
+            if (e != cudaSuccess)
+                return e;
+        }
+        cfg.gridDim = dim3(pl.groups, pl.col_tiles, 1);
+        cfg.blockDim = dim3(kGenBwdGroups, pl.lanes, 1);
+        cfg.dynamicSmemBytes = pl.smem;
+        e = cudaLaunchKernelEx(&cfg, bwd_generic_kernel, a, pl.rows_per_group, p.n_tokens,
+                               static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
+                               static_cast<uint16_t *>(p.dscore), partial);
+    }
     if (e != cudaSuccess)
         return e;
-    return launch_dape_finalize(partial, pl.groups, (int64_t)p.ratio * p.coff * p.head_dim, p.dape, st);
+    return launch_dape_finalize(partial, n_partials, (int64_t)p.ratio * p.coff * p.head_dim, p.dape, st);
 }
 
 }  // namespace csa

@@ -2,6 +2,7 @@
 // files.  Not installed, not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -108,16 +109,27 @@ struct GenericPlan {
     size_t smem;            // backward shared memory (grad_ape slots)
     int64_t partial_floats; // workspace floats
     int num_sms;
+    int staged_blocks;      // > 0: the shared-memory staged kernels, this many row blocks (= partials)
 };
 bool generic_supported(int ratio, int coff, int head_dim);
-GenericPlan plan_generic(int ratio, int coff, int head_dim, int capacity, int num_sms);
-cudaError_t launch_fwd_generic(const FwdParams &p, int num_sms, cudaStream_t st);
-cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float *partial, cudaStream_t st);
+cudaError_t plan_generic(int ratio, int coff, int head_dim, int capacity, int num_sms, GenericPlan *pl);
+cudaError_t launch_fwd_generic(const FwdParams &p, unsigned *status, int num_sms, cudaStream_t st);
+cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float *partial, unsigned *status,
+                               cudaStream_t st);
 
 // Raises a kernel's dynamic shared-memory limit (a per-function attribute shared
 // by all its launch configurations) to the current device's maximum, once per
 // (device, kernel).
 cudaError_t allow_max_smem(const void *fn);
+
+// Blocks of a kernel configuration resident on the whole current device (blocks of
+// `cluster`-block clusters: whole clusters only), with allow_max_smem applied to the
+// kernel first; cached per (device, kernel, threads, shared memory, cluster).
+cudaError_t resident_blocks(const void *fn, int threads, size_t smem, int cluster, int *resident);
+
+// Tiled TMA map of a [rows, C] bf16 row-major tensor at ptr with [box_rows x
+// box_cols] boxes (no swizzle, 256-byte L2 promotion).
+cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int box_cols, int box_rows);
 
 // Records a status and the thread-local message returned by csa_last_error_message().
 int fail_status(int status, const char *fmt, ...);

@@ -131,7 +131,9 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
             return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
         floats = (int64_t)partials * ratio * coff * head_dim;
     } else if (generic) {
-        gp = csa::plan_generic(ratio, coff, head_dim, capacity, nd->num_sms);
+        e = csa::plan_generic(ratio, coff, head_dim, capacity, nd->num_sms, &gp);
+        if (e != cudaSuccess)
+            return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
         floats = gp.partial_floats;
     } else if (streamed) {
         sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, nd->num_sms);
@@ -152,7 +154,7 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
     if (r128)
         e = csa::launch_bwd_r128(p, nd->scratch, r128_blocks, nd->status, st);
     else if (generic)
-        e = csa::launch_bwd_generic(p, gp, nd->scratch, st);
+        e = csa::launch_bwd_generic(p, gp, nd->scratch, nd->status, st);
     else if (streamed)
         e = csa::launch_bwd_stream(p, sp, nd->scratch, nd->status, st);
     else

@@ -33,7 +33,6 @@
 // the status word, the kernel then stops and exits normally).
 #include <cooperative_groups.h>
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <mutex>
 
@@ -703,40 +702,10 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
 
 // ------------------------------------------------------------------- host
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t *err)
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static cudaError_t e = cudaSuccess;
-    std::call_once(once, []() {
-        cudaDriverEntryPointQueryResult q;
-        void *p = nullptr;
-        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
-        if (e == cudaSuccess && q != cudaDriverEntryPointSuccess)
-            e = cudaErrorNotSupported;
-        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    *err = e;
-    return fn;
-}
-
-// Tensor map of a [rows, C] bf16 row-major tensor with [128 x tc] boxes.  The row
-// extent is the int32 flat-offset bound, not the (unknown to the forward) token
-// count: every box the kernels request lies inside a real block.
+// Tensor map of a [rows, C] bf16 row-major tensor with [128 x tc] boxes.
 cudaError_t make_map(CUtensorMap *m, const void *ptr, int64_t C, int tc)
 {
-    cudaError_t e;
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn(&e);
-    if (e != cudaSuccess)
-        return e;
-    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)(((int64_t)1 << 31) / C)};
-    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)tc, (cuuint32_t)kR};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    return make_tensor_map_2d(m, ptr, C, tc, kR);
 }
 
 struct R128Plan {

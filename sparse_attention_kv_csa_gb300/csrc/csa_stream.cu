@@ -156,17 +156,6 @@ struct Lanes {
     int lc;    // this thread's first column in the tile
 };
 
-// Next slot of a row lane: `step` slots on, the phase flipping on each wrap
-// (stages is a multiple of step).
-__device__ __forceinline__ void ring_next(int &st, uint32_t &ph, int step, int stages)
-{
-    st += step;
-    if (st >= stages) {
-        st -= stages;
-        ph ^= 1u;
-    }
-}
-
 __device__ __forceinline__ Lanes lanes_of(const StreamArgs &a, int warp, int lane)
 {
     Lanes l;
@@ -229,49 +218,6 @@ __host__ size_t smem_bytes(int stages, int stage_bytes, size_t red_bytes)
 }
 
 // ---------------------------------------------------------------- producer
-
-// Row -> window map for a producer's increasing rows.  The offsets of the
-// current segment stay in registers, so the next row of the same segment costs
-// no load; the binary search (dependent loads, slow under a full memory system)
-// runs once per segment change.  Same result as map_row.
-struct RowCursor {
-    int r0, r1;            // real rows: [cc[0], cc[n_seg])
-    int lo, hi, tok;       // current segment: rows [lo, hi), first token tok
-    int seg;
-};
-
-__device__ __forceinline__ void cursor_init(RowCursor &c, const int32_t *__restrict__ cc, int n_seg)
-{
-    c.r0 = n_seg > 0 ? __ldg(cc) : 0;
-    c.r1 = n_seg > 0 ? __ldg(cc + n_seg) : 0;
-    c.lo = c.hi = 0;
-    c.tok = 0;
-    c.seg = -1;
-}
-
-__device__ __forceinline__ RowMap cursor_map(RowCursor &c, int r, const int32_t *__restrict__ cu,
-                                             const int32_t *__restrict__ cc, int n_seg, int ratio)
-{
-    RowMap m;
-    m.base = 0;
-    m.seg = -1;
-    m.real = false;
-    m.first = true;
-    if (r < c.r0 || r >= c.r1)
-        return m;
-    if (c.seg < 0 || r < c.lo || r >= c.hi) {
-        c.seg = find_segment(cc, n_seg, r);
-        c.lo = __ldg(cc + c.seg);
-        c.hi = __ldg(cc + c.seg + 1);
-        c.tok = __ldg(cu + c.seg);
-    }
-    const int b = r - c.lo;
-    m.base = (int64_t)c.tok + (int64_t)b * ratio;
-    m.seg = c.seg;
-    m.real = true;
-    m.first = (b == 0);
-    return m;
-}
 
 // Issues the copies of rows row0, row0 + rstride, ... < rend.  Runs on one lane.
 template <int RATIO, int COFF, bool BWD>
@@ -691,89 +637,13 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     return pl;
 }
 
-// Resident blocks of a kernel configuration, computed once per (device, kernel,
-// block size, shared memory, cluster) and cached: the occupancy queries and the
-// shared-memory attribute are host calls too slow to repeat on every launch.
-struct ResidentKey {
-    int dev;
-    const void *fn;
-    int threads;
-    size_t smem;
-    int cluster;
-};
-
-static cudaError_t cached_resident(const ResidentKey &k, int *resident, cudaError_t (*query)(const ResidentKey &, int *))
-{
-    static std::mutex mu;
-    static ResidentKey keys[64];
-    static int vals[64];
-    static int n = 0;
-    {
-        std::lock_guard<std::mutex> g(mu);
-        for (int i = 0; i < n; ++i)
-            if (keys[i].dev == k.dev && keys[i].fn == k.fn && keys[i].threads == k.threads &&
-                keys[i].smem == k.smem && keys[i].cluster == k.cluster) {
-                *resident = vals[i];
-                return cudaSuccess;
-            }
-    }
-    cudaError_t e = query(k, resident);
-    if (e != cudaSuccess)
-        return e;
-    std::lock_guard<std::mutex> g(mu);
-    if (n < 64) {
-        keys[n] = k;
-        vals[n] = *resident;
-        ++n;
-    }
-    return cudaSuccess;
-}
-
-static cudaError_t query_resident(const ResidentKey &k, int *resident)
-{
-    // The kernel's dynamic shared-memory limit is a per-function attribute shared by
-    // every configuration: raise it to the device maximum (not to this plan's size,
-    // which a later plan of another head_dim could undercut).
-    cudaError_t e = allow_max_smem(k.fn);
-    if (e != cudaSuccess)
-        return e;
-    if (k.cluster > 1) {
-        // clusters are placed within GPCs: ask how many fit, not blocks per SM
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(k.cluster, 1, 1);
-        cfg.blockDim = dim3(k.threads, 1, 1);
-        cfg.dynamicSmemBytes = k.smem;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = k.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, k.fn, &cfg);
-        *resident = clusters * k.cluster;
-        return e;
-    }
-    int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, k.threads, k.smem);
-    if (e == cudaSuccess)
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, k.dev);
-    *resident = per_sm * sms;
-    return e;
-}
-
 template <int RATIO, int COFF>
 static cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out)
 {
     const void *fn = bwd ? reinterpret_cast<const void *>(bwd_stream_kernel<RATIO, COFF>)
                          : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF>);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return e;
     int resident = 0;
-    e = cached_resident(ResidentKey{dev, fn, pl.threads, pl.smem, pl.cluster}, &resident, query_resident);
+    cudaError_t e = resident_blocks(fn, pl.threads, pl.smem, pl.cluster, &resident);
     if (e != cudaSuccess)
         return e;
     int blocks = (resident > 0 ? resident : 1) / pl.tiles;

@@ -83,3 +83,47 @@ def test_generic_workload(csa):
     c = w.WORKLOADS["r16c2d512_8x4096"]()
     check(c, csa)
     assert csa.csa_device_status() == 0
+
+
+# ------------------------------------------- shared-memory staged kernels
+# head_dim a multiple of 128 and windows of at most 64 positions (coff * ratio)
+# take the staged kernels (TMA boxes into a shared-memory ring); wider windows
+# stay on the global-memory walk.
+
+@pytest.mark.parametrize("ratio", [1, 2, 3, 5, 8, 16, 31, 64])
+@pytest.mark.parametrize("coff", [1, 2])
+@pytest.mark.parametrize("li", range(3))
+def test_staged_ratio_bitwise(csa, ratio, coff, li):
+    lens = layout(ratio, li)
+    head_dim = (128, 256, 384)[li]
+    leading = (0, 3, 0)[li]
+    pad = (0, 0, 5)[li]
+    T = leading + sum(lens) + pad
+    c = w.make_case("gst", ratio, coff, head_dim, lens, extra_rows=(2, 0, 1)[li], n_tokens=T, leading=leading,
+                    seed=200 * ratio + 10 * coff + li)
+    check(c, csa)
+
+
+def test_staged_many_rows_per_block(csa):
+    """10000 rows on one column tile: every ring slot is reused many times."""
+    c = w.make_case("gstmany", 8, 2, 128, [80003, 8 * 7 + 1], extra_rows=5, seed=31)
+    check(c, csa)
+
+
+def test_staged_deterministic_and_edges(csa):
+    c = w.make_case("gsdet", 12, 2, 128, [3000, 11, 970], extra_rows=2, seed=19)
+    d = Dev(c)
+    assert np.array_equal(run_fwd(d, csa, canary=0xFFFF), run_fwd(d, csa, canary=0x7FC1))
+    b1 = run_bwd(d, csa, canary=0xFFFF, dape_fill=float("nan"))
+    b2 = run_bwd(d, csa, canary=0x7FC1, dape_fill=3.0)
+    assert np.array_equal(b1[0], b2[0]) and np.array_equal(b1[1], b2[1])
+    assert np.array_equal(b1[2].view(np.uint32), b2[2].view(np.uint32))
+    c = w.make_case("gscap0", 6, 2, 128, [5, 3], capacity=0, seed=3)
+    dkv, dsc, dape = run_bwd(Dev(c), csa, capacity=0)
+    assert not dkv.any() and not dsc.any() and not dape.any()
+    c = w.make_case("gspad", 6, 2, 256, [5, 3, 4], extra_rows=2, seed=4)
+    d = Dev(c)
+    assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))
+    dkv, dsc, dape = run_bwd(d, csa)
+    assert not dkv.any() and not dsc.any() and not dape.any()
+    assert csa.csa_device_status() == 0

@@ -13,7 +13,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("ratio,coff,head_dim,lens", [(4, 2, 512, [4096, 37, 3]), (4, 2, 64, [300, 9]),
                                                       (128, 1, 512, [4096, 300]), (128, 2, 128, [1000]),
-                                                      (16, 2, 512, [900, 17]), (7, 1, 64, [300, 5])])
+                                                      (16, 2, 512, [900, 17]), (7, 1, 64, [300, 5]),
+                                                      (3, 2, 256, [700, 5])])
 def test_capture_and_replay_bitwise(ratio, coff, head_dim, lens):
     import torch
     import sparse_attention_kv_csa_gb300 as csa
