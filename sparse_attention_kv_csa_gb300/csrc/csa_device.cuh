@@ -32,6 +32,17 @@ __device__ __forceinline__ float max_nan(float a, float b)
     return d;
 }
 
+// Three-input form (sm_100 and later): NaN if any input is NaN, else the largest.
+// The maximum of a set does not depend on the grouping, so a window's max may be
+// taken three values at a time (a zero's sign may differ, which no use of the
+// max can see: s - m and EXP treat +0 and -0 alike).
+__device__ __forceinline__ float max3_nan(float a, float b, float c)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // ----------------------------------------------------------- reciprocal
 // 1/d rounded to nearest for d in [2^-8, 2^8], which holds every softmax
 // denominator here: at most 256 terms, the largest 1 or within a few ulp of it

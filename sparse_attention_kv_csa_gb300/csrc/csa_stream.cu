@@ -307,29 +307,53 @@ __device__ __forceinline__ void stage_words(uint32_t (&w)[kNP], const unsigned c
     ld_np(w, stage + stage_offset<RATIO, COFF>(arr, p, i, rw) + (p * pcol + lc) * 2);
 }
 
+// Max over a row's valid window positions, three values at a time: the own
+// block's part, then (coff 2, unless the row is a segment's first block) the
+// previous block's part folded in.
+template <int RATIO, int COFF>
+__device__ __forceinline__ float window_max(const float (&v)[COFF * RATIO], bool first)
+{
+    constexpr int W = COFF * RATIO, K0 = (COFF - 1) * RATIO;
+    float a = v[K0];
+#pragma unroll
+    for (int k = K0 + 1; k < W; k += 2)
+        a = k + 1 < W ? max3_nan(a, v[k], v[k + 1]) : max_nan(a, v[k]);
+    if (COFF == 1)
+        return a;
+    float b = a;
+#pragma unroll
+    for (int i = 0; i < RATIO; i += 2)
+        b = i + 1 < RATIO ? max3_nan(b, v[i], v[i + 1]) : max_nan(b, v[i]);
+    return first ? a : b;
+}
+
 template <int RATIO, int COFF>
 __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, int pcol, int lc, bool first,
                                            const ApeRegs<RATIO, COFF> &ap, uint32_t (&kvw)[COFF * RATIO][kNP],
                                            float2 (&e)[COFF * RATIO][kNP], float2 (&den)[kNP], float2 (&num)[kNP])
 {
     constexpr int W = COFF * RATIO;
-    float2 m[kNP];
-#pragma unroll
-    for (int q = 0; q < kNP; ++q)
-        m[q] = make_float2(-INFINITY, -INFINITY);
+    // Every position is read; a first block's previous-block positions hold stale
+    // stage bytes, which the max below and the sums skip.
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-        if (COFF == 2 && k < RATIO && first)
-            continue;
         uint32_t sw[kNP];
         stage_words<RATIO, COFF>(sw, stage, 1, k, rw, pcol, lc);
         stage_words<RATIO, COFF>(kvw[k], stage, 0, k, rw, pcol, lc);
 #pragma unroll
-        for (int q = 0; q < kNP; ++q) {
+        for (int q = 0; q < kNP; ++q)
             e[k][q] = add2(bf16x2_to_f2(sw[q]), ap.v[k][q]);
-            m[q].x = max_nan(m[q].x, e[k][q].x);
-            m[q].y = max_nan(m[q].y, e[k][q].y);
+    }
+    float2 m[kNP];
+#pragma unroll
+    for (int q = 0; q < kNP; ++q) {
+        float vx[W], vy[W];
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            vx[k] = e[k][q].x;
+            vy[k] = e[k][q].y;
         }
+        m[q] = make_float2(window_max<RATIO, COFF>(vx, first), window_max<RATIO, COFF>(vy, first));
     }
     float2 negm[kNP];
 #pragma unroll
