@@ -111,6 +111,33 @@ __device__ __forceinline__ float2 exp2lanes(float2 x)
 }
 
 // ----------------------------------------------------------------- bf16
+// Mixed-precision forms (sm_100 and later) that take bf16 operands as they are.
+// Widening bf16 to fp32 is exact, so each equals its fp32 counterpart on the
+// widened values bit for bit, without the two unpacking permutes per word.
+// w, gw, kw: words of two bf16 (low half = lower column).
+
+// f32(w) + a, each lane rounded once to nearest: add2(bf16x2_to_f2(w), a).
+__device__ __forceinline__ float2 add2_bf16x2(uint32_t w, float2 a)
+{
+    float2 d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(w), "f"(a.x), "f"(a.y));
+    return d;
+}
+
+// f32(gw) * f32(kw) + c, each lane rounded once: fma2(bf16x2_to_f2(gw), bf16x2_to_f2(kw), c).
+__device__ __forceinline__ float2 fma2_bf16x2(uint32_t gw, uint32_t kw, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b16 g0, g1, k0, k1;\n\tmov.b32 {g0, g1}, %2;\n\tmov.b32 {k0, k1}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, g0, k0, %4;\n\tfma.rn.f32.bf16 %1, g1, k1, %5;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(gw), "r"(kw), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 // A 32-bit word holding two bf16 (low half = lower column) <-> an fp32 pair.
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w)
 {

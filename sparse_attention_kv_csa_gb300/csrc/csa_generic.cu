@@ -123,7 +123,7 @@ __device__ __forceinline__ void gen_pool(const GenArgs &a, const RowMap &rm, int
                 if (i0 + u < a.ratio)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const float2 s = add2(bf16x2_to_f2(sw[u][h]), av[u][h]);
+                        const float2 s = add2_bf16x2(sw[u][h], av[u][h]);
                         m[h].x = max_nan(m[h].x, s.x);
                         m[h].y = max_nan(m[h].y, s.y);
                     }
@@ -153,7 +153,7 @@ __device__ __forceinline__ void gen_pool(const GenArgs &a, const RowMap &rm, int
                 if (i0 + u < a.ratio)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const float2 e = exp2lanes(add2(add2(bf16x2_to_f2(sw[u][h]), av[u][h]), negm[h]));
+                        const float2 e = exp2lanes(add2(add2_bf16x2(sw[u][h], av[u][h]), negm[h]));
                         den[h] = add2(den[h], e);
                         num[h] = fma2(e, bf16x2_to_f2(kw[u][h]), num[h]);
                     }
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kGenBwdGroups * kGenBwdMaxLanes, 2)
                     float2 ds[2];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const float2 e = exp2lanes(add2(add2(bf16x2_to_f2(sw[u][h]), av[u][h]), negm[h]));
+                        const float2 e = exp2lanes(add2(add2_bf16x2(sw[u][h], av[u][h]), negm[h]));
                         const float2 pk = mul2(e, inv[h]);
                         dk[h] = f2_to_bf16x2(mul2(g[h], pk));
                         ds[h] = mul2(pk, add2(mul2(g[h], bf16x2_to_f2(kw[u][h])), ngo[h]));
@@ -461,7 +461,7 @@ __device__ __forceinline__ void gs_load_ape(const GenArgs &g, float *apet, int c
 __device__ __forceinline__ float2 gs_logits(const unsigned char *sc, const float *ap, int k)
 {
     const uint32_t w = *reinterpret_cast<const uint32_t *>(sc + k * (kGsTile * 2));
-    return add2(bf16x2_to_f2(w), *reinterpret_cast<const float2 *>(ap + k * kGsTile));
+    return add2_bf16x2(w, *reinterpret_cast<const float2 *>(ap + k * kGsTile));
 }
 
 // Passes 1 and 2 over the staged window (positions k0 .. W-1 of at most WMAX):

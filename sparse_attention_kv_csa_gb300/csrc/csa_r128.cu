@@ -250,8 +250,8 @@ __device__ __forceinline__ void r128_load(const unsigned char *stage, int c, int
         const int off = tok * Geo<COFF>::TC * 2 + 8 * g;
         cs.kv[i] = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(0, part) + off);
         const uint2 sw = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(1, part) + off);
-        cs.e[i][0] = add2(bf16x2_to_f2(sw.x), ap[i][0]);
-        cs.e[i][1] = add2(bf16x2_to_f2(sw.y), ap[i][1]);
+        cs.e[i][0] = add2_bf16x2(sw.x, ap[i][0]);
+        cs.e[i][1] = add2_bf16x2(sw.y, ap[i][1]);
     }
 }
 
@@ -594,6 +594,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
             if (!r128_pool<COFF, LEAN>(s, buf, c, g, ok, ok && m.real, first, cs, stage))
                 break;
             const float2 gg[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
+            const uint32_t gwq[2] = {gw.x, gw.y};
             float *fin = s.fin + (size_t)buf * 2 * G::TC;
             {
                 int j;
@@ -638,7 +639,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
                 for (int q = 0; q < 2; ++q) {
                     const float2 pk = mul2(cs.e[i][q], inv[q]);
                     dk[q] = f2_to_bf16x2(mul2(gg[q], pk));
-                    const float2 ds = mul2(pk, fma2(gg[q], bf16x2_to_f2(kw[q]), ngo[q]));
+                    const float2 ds = mul2(pk, fma2_bf16x2(gwq[q], kw[q], ngo[q]));
                     dsw[q] = f2_to_bf16x2(ds);
                     acc[i][q] = add2(acc[i][q], ds);
                 }

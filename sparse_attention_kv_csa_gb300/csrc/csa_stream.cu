@@ -342,7 +342,7 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, i
         stage_words<RATIO, COFF>(kvw[k], stage, 0, k, rw, pcol, lc);
 #pragma unroll
         for (int q = 0; q < kNP; ++q)
-            e[k][q] = add2(bf16x2_to_f2(sw[q]), ap.v[k][q]);
+            e[k][q] = add2_bf16x2(sw[q], ap.v[k][q]);
     }
     float2 m[kNP];
 #pragma unroll

@@ -86,6 +86,34 @@ def test_overflow_nan_masks(csa):
     check_against_oracle(w.WORKLOADS["stress_overflow"](), csa, overflow=True)
 
 
+@pytest.mark.parametrize("ratio", [4, 8])
+@pytest.mark.parametrize("order", ["ascending", "shuffled"])
+def test_every_bf16_score_pattern_bitwise(csa, ratio, order):
+    """The kernels add the bf16 score to the fp32 APE with the mixed-precision add
+    (bf16 operand taken as it is).  Every one of the 65536 bf16 bit patterns --
+    signed zeros, subnormals, the largest finite values, infinities, NaNs -- as a
+    score, against APE columns holding zeros, signed subnormals and normal values,
+    gives the oracle's bits in out, grad_kv and grad_score (NaN-aware), on the
+    ratio-4 stream kernels and the staged generic kernels (ratio 8)."""
+    D, C = 128, 256
+    T = 65536 // C
+    c = w.make_case("allbf16", ratio, 2, D, [T], extra_rows=1, seed=11 + ratio)
+    pat = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    if order == "shuffled":
+        pat = pat[np.argsort(w.uniform01(ratio, 7, 65536), kind="stable")]
+    c.score = pat.reshape(T, C).copy()
+    ape = c.ape.copy()
+    ape[:, 0::4] = 0.0
+    ape[:, 1::8] = np.float32(1e-40)
+    ape[:, 5::8] = np.float32(-3e-42)
+    c.ape = ape
+    d = Dev(c)
+    assert same_bits_nan_aware(run_fwd(d, csa), oracle.case_fwd_f32(c))
+    dkv, dsc, _ = run_bwd(d, csa)
+    want = oracle.case_bwd_f32(c)
+    assert same_bits_nan_aware(dkv, want[0]) and same_bits_nan_aware(dsc, want[1])
+
+
 def test_x64_scaling_is_exact_on_gpu(csa):
     """The kernels' outputs scale exactly 2^6 (out, grad_kv) and 2^12 (grad_score,
     grad_ape) when kv and grad_out are scaled by 64 (Numerics, point 2)."""
