@@ -382,7 +382,9 @@ size_t gs_smem_bytes(int stages, int stage_bytes, int W, int lanes, bool bwd)
 __device__ __forceinline__ GsSmem gs_carve(unsigned char *raw, int stages, int stage_bytes, int W)
 {
     GsSmem s;
-    unsigned char *p = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 127) & ~uintptr_t(127));
+    // 128-byte aligned stages (TMA destinations), by an offset from the shared
+    // array (no integer round trip: the pointers stay shared-memory pointers)
+    unsigned char *p = raw + ((128u - (smem_addr(raw) & 127u)) & 127u);
     s.stages = p;
     p += (size_t)stages * stage_bytes;
     s.meta = reinterpret_cast<GsMeta *>(p);
@@ -467,18 +469,40 @@ __device__ __forceinline__ float2 gs_logits(const unsigned char *sc, const float
 // Passes 1 and 2 over the staged window (positions k0 .. W-1 of at most WMAX):
 // the logits, then e = EXP(s - m) in place, in registers (the window loop is
 // unrolled to WMAX, positions outside [k0, W) skipped); m, den, num.
-template <int WMAX>
+// TREE (the forward): the maximum is taken over all WMAX slots, positions outside
+// [k0, W) holding -inf, in three interleaved chains of three-input maxima joined
+// at the end -- the maximum of a set does not depend on the grouping (NaN if any
+// is NaN), and three short chains instead of one of W dependent steps keep the
+// warp issuing.  The backward, short of registers, keeps the single chain.
+template <int WMAX, bool TREE>
 __device__ __forceinline__ void gs_pool(const unsigned char *kvp, const unsigned char *sc, const float *ap, int k0,
                                         int W, float2 (&e)[WMAX], float2 &m, float2 &den, float2 &num)
 {
-    m = make_float2(-INFINITY, -INFINITY);
+    if constexpr (TREE) {
 #pragma unroll
-    for (int k = 0; k < WMAX; ++k)
-        if (k >= k0 && k < W) {
-            e[k] = gs_logits(sc, ap, k);
-            m.x = max_nan(m.x, e[k].x);
-            m.y = max_nan(m.y, e[k].y);
+        for (int k = 0; k < WMAX; ++k)
+            e[k] = (k >= k0 && k < W) ? gs_logits(sc, ap, k) : make_float2(-INFINITY, -INFINITY);
+        float2 mc[3];
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            mc[i] = make_float2(-INFINITY, -INFINITY);
+#pragma unroll
+        for (int k = 0; k < WMAX; k += 2) {
+            float2 &a = mc[(k / 2) % 3];
+            a.x = max3_nan(a.x, e[k].x, e[k + 1].x);
+            a.y = max3_nan(a.y, e[k].y, e[k + 1].y);
         }
+        m = make_float2(max3_nan(mc[0].x, mc[1].x, mc[2].x), max3_nan(mc[0].y, mc[1].y, mc[2].y));
+    } else {
+        m = make_float2(-INFINITY, -INFINITY);
+#pragma unroll
+        for (int k = 0; k < WMAX; ++k)
+            if (k >= k0 && k < W) {
+                e[k] = gs_logits(sc, ap, k);
+                m.x = max_nan(m.x, e[k].x);
+                m.y = max_nan(m.y, e[k].y);
+            }
+    }
     const float2 negm = make_float2(-m.x, -m.y);
     den = num = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -532,7 +556,7 @@ __global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
         const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes + lc * 2;
         const int k0 = (g.coff == 2 && s.meta[st].first) ? g.ratio : 0;
         float2 e[WMAX], m, den, num;
-        gs_pool<WMAX>(stage, stage + sc_off, s.apet + lc, k0, W, e, m, den, num);
+        gs_pool<WMAX, true>(stage, stage + sc_off, s.apet + lc, k0, W, e, m, den, num);
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
@@ -624,7 +648,7 @@ __global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
             const float *ap = s.apet + lc;
             const int k0 = (g.coff == 2 && m.first) ? g.ratio : 0;
             float2 e[WMAX], mx, den, num;
-            gs_pool<WMAX>(kvp, sc, ap, k0, W, e, mx, den, num);
+            gs_pool<WMAX, false>(kvp, sc, ap, k0, W, e, mx, den, num);
             const float2 gg = bf16x2_to_f2(*reinterpret_cast<const uint32_t *>(stage + go_off + lc * 2));
             const float2 inv = make_float2(recip_den(den.x), recip_den(den.y));
             const float2 go = mul2(gg, mul2(num, inv));

@@ -74,6 +74,7 @@ struct StreamPlan {
     int tiles;           // head_dim / tc (gridDim.y)
     int row_lanes;       // rows in flight per block (tc / 128 column warps each)
     bool whole;          // stage whole token rows (one column tile)
+    bool tma;            // stage the tile with one 2-D TMA box per array and part (tc <= 256)
     int threads;         // consumer warps + one producer warp, x 32
     int stage_bytes;     // bytes per ring stage
     int stages;          // ring depth

@@ -414,6 +414,21 @@ __device__ __forceinline__ void r128_final(const R128Smem<COFF> &s, int buf, int
     }
 }
 
+// The dynamic shared memory's base aligned to 1 KB (TMA tensor destinations need
+// 128 bytes; the plans reserve 1 KB of slack).  OFFSET: as an offset added to the
+// shared array, so the compiler keeps shared-memory addressing for every pointer
+// derived from it -- faster in the forwards and the lean backward.  Otherwise
+// through an integer round trip, which the register-resident coff-1 backward
+// measured faster with (it then fits its 168 registers without a spill).
+template <bool OFFSET>
+__device__ __forceinline__ unsigned char *align_1k(unsigned char *raw)
+{
+    if constexpr (OFFSET)
+        return raw + ((1024u - (smem_addr(raw) & 1023u)) & 1023u);
+    else
+        return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+}
+
 template <int COFF>
 __device__ __forceinline__ void r128_init(const R128Smem<COFF> &s, int stages)
 {
@@ -437,10 +452,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
 {
     using G = Geo<COFF>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // TMA tensor destinations need 128-byte alignment; the base is aligned to 1 KB
-    // by hand (the plan reserves 1 KB of slack for this).
-    unsigned char *smem_base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                                 ~uintptr_t(1023));
+    unsigned char *smem_base = align_1k<true>(smem_raw);
     const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes, false);
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -513,11 +525,8 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
 {
     using G = Geo<COFF>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // TMA tensor destinations need 128-byte alignment; the base is aligned to 1 KB
-    // by hand (the plan reserves 1 KB of slack for this).
-    unsigned char *smem_base = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                                 ~uintptr_t(1023));
     constexpr bool LEAN = kBwdLean<COFF>;
+    unsigned char *smem_base = align_1k<LEAN>(smem_raw);
     const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes, LEAN);
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -726,8 +735,11 @@ R128Plan r128_plan(bool bwd, int head_dim)
     pl.stages = bwd && !tile ? 4 : 2;
     pl.threads = G::THREADS;
     pl.tiles = head_dim / G::TC;
-    // lean backward: pairs of blocks merge their grad_ape partials (half as many)
-    pl.cluster = bwd ? (tile ? 2 : CSA_R128_BWD_CLUSTER) : 1;
+    // no clusters for the lean backward: pairs of blocks would halve the grad_ape
+    // partials, but the grid must then be an even number of blocks per column
+    // tile, which leaves SMs idle (19 blocks per tile fill 152 SMs twice over at
+    // head_dim 512)
+    pl.cluster = bwd ? (tile ? 1 : CSA_R128_BWD_CLUSTER) : 1;
     pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes, tile) + 1024;  // + alignment slack
     if (bwd) {  // grad_ape staging reuses the stages: make sure it fits
         const size_t red = (size_t)kR * COFF * G::TC * sizeof(float);
