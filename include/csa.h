@@ -140,14 +140,16 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * could block, a plug-in that may not use the CUDA allocator.
  *
  * Same arguments, results and errors as csa_compress_bwd (bitwise the same
- * outputs), except that the grad_ape partial sums go to a fixed 6 MiB array in
+ * outputs, but see below for ratio 128's grad_ape), except that the grad_ape partial sums go to a fixed 6 MiB array in
  * the library's device code instead of the library's memory pool.  That array
  * occupies 6 MiB on every GPU that loads the library, until the process exits.
- * A shape that needs more partial storage than the array holds is rejected with
- * CSA_ERR_TOO_LARGE before anything is launched (on a 152-SM GB300 every shape
- * fits except ratio 128 with coff 2 and head_dim above 6144, and other ratios
- * with ratio * coff * head_dim above 1572864).  No cudaMalloc,
- * cudaFree or other allocating call is made.
+ * Where the regular backward's grid would need more partial storage than the
+ * array holds, ratio 128 runs with fewer row blocks (same grad_kv / grad_score
+ * bits; grad_ape summed in another fixed grouping); a shape whose single partial
+ * does not fit is rejected with CSA_ERR_TOO_LARGE before anything is launched (on
+ * a 152-SM GB300 every shape fits except ratio 128 with coff 2 and head_dim above
+ * 6144, and other ratios with ratio * coff * head_dim above 1572864).  No
+ * cudaMalloc, cudaFree or other allocating call is made.
  *
  * Every call on a device shares the array and leaves its contents behind; each
  * call writes all it reads, so nothing needs clearing, but calls that overlap on

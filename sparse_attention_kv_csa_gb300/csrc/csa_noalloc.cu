@@ -26,7 +26,9 @@
 // Scratch for the grad_ape partials: 1572864 floats = 6 MiB per GPU.  On a
 // 152-SM GB300 every shape fits except ratio 128 with coff 2 and head_dim above
 // 6144, and other ratios with ratio * coff * head_dim above 1572864, which are
-// rejected.
+// rejected.  Ratio 128 runs with fewer row blocks than the regular backward
+// where a full grid's partials would not fit (coff 2: 12 per column tile at
+// head_dim 512 instead of 19).
 static constexpr size_t kScratchFloats = 1536u * 1024u;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 // Status word of the bounded waits of calls made through this entry point.
@@ -130,6 +132,15 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
         if (e != cudaSuccess)
             return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
         floats = (int64_t)partials * ratio * coff * head_dim;
+        // More partials than the array holds: fewer row blocks per column tile
+        // (each walks more rows; one partial per cluster of blocks).
+        const int64_t per = (int64_t)ratio * coff * head_dim;
+        if (floats > (int64_t)kScratchFloats && per <= (int64_t)kScratchFloats && partials > 0) {
+            const int cluster = r128_blocks / partials;
+            const int fit = (int)((int64_t)kScratchFloats / per);
+            r128_blocks = fit * cluster;
+            floats = (int64_t)fit * per;
+        }
     } else if (generic) {
         e = csa::plan_generic(ratio, coff, head_dim, capacity, nd->num_sms, &gp);
         if (e != cudaSuccess)

@@ -75,6 +75,20 @@ def test_noalloc_ratio128_matches_backward(csa):
         assert np.abs(got[2] - want[2]).max() <= 1e-5 * np.abs(want[2]).max()
 
 
+def test_noalloc_ratio128_overlapping_window_fits_with_fewer_blocks(csa):
+    """ratio 128, coff 2, head_dim 512: the regular backward's grid (19 row blocks
+    per column tile) would need 19 grad_ape partials of 128 x 1024 floats, more
+    than the fixed array; the no-alloc call runs 12 row blocks instead.  grad_kv
+    and grad_score keep their bits; grad_ape is the same sum in another grouping."""
+    c = w.make_case("na128c2", 128, 2, 512, [4096, 1500], extra_rows=3, seed=9)
+    d = Dev(c)
+    want = run_bwd(d, csa)
+    for canary in (0xFFFF, 0x7FC1):
+        got = run_noalloc(d, csa, canary)
+        assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
+        assert np.abs(got[2] - want[2]).max() <= 1e-5 * np.abs(want[2]).max()
+
+
 def test_noalloc_rejects_shape_beyond_its_scratch(csa):
     """ratio 128, coff 2, head_dim 8192: one grad_ape partial is 128 x 16384 floats
     (8 MiB), more than the fixed 6 MiB array holds: rejected before launch."""
