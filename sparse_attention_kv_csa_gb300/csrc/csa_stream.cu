@@ -12,9 +12,11 @@
 // Structure (per thread block, persistent over the rows b, b + gridDim.x, ...):
 //   * one producer warp: for each row, waits for a free stage of a shared-memory
 //     ring, then issues raw bulk copies (cp.async.bulk) of every window row the
-//     output row reads -- each (token, half) is one contiguous run of TC*2 bytes --
-//     and, in the backward, the grad_out row; completion is counted in bytes on the
-//     stage's "full" mbarrier;
+//     output row reads -- each (token, half) is one contiguous run of TC*2 bytes;
+//     whole token rows for a narrow single-tile head; one 2-D TMA box per array
+//     and part for the narrow tiles of a multi-tile head -- and, in the backward,
+//     the grad_out row; completion is counted in bytes on the stage's "full"
+//     mbarrier;
 //   * consumer warps: thread t owns columns [c0 + 2*kNP*t, c0 + 2*kNP*(t + 1)) of
 //     the block's column tile (kNP fp32 pairs, two by default) for every row, so
 //     its APE values stay in registers; it waits on
