@@ -64,15 +64,23 @@ def parse_args():
 def algorithmic_bytes(c):
     """Bytes each pass must move (each consumed kv/score slot read once; the
     eager window materialisation is not counted).
-    forward:  kv + score of every consumed slot, ape, out (all capacity rows)
-    backward: kv + score of every consumed slot, grad_out of real rows, ape,
-              dkv + dscore written in full (n_tokens rows), dape written."""
+    forward:  kv + score of every slot a row reads (padding rows included), ape,
+              out (all capacity rows)
+    backward: kv + score of every slot a real row reads, grad_out of real rows,
+              ape, dkv + dscore written in full (n_tokens rows), dape written."""
     nb = [L // c.ratio for L in c.seqlens]
     consumed_rows = sum(b + (max(b - 1, 0) if c.coff == 2 else 0) for b in nb)  # half-rows of D
     win = 4 * c.head_dim * c.ratio * consumed_rows
+    # Padding rows (forward only) read the own half of tokens [0, ratio): counted
+    # where no real row's own block already covers them.
+    pad = 0
+    if c.capacity > c.n_real_rows:
+        cu = [int(x) for x in c.cu_seqlens]
+        covered = sum(max(0, min(c.ratio, cu[s] + nb[s] * c.ratio) - max(0, cu[s])) for s in range(len(nb)))
+        pad = 4 * c.head_dim * (c.ratio - covered)
     C = c.coff * c.head_dim
     ape = 4 * c.ratio * C
-    fwd = win + ape + 2 * c.capacity * c.head_dim
+    fwd = win + pad + ape + 2 * c.capacity * c.head_dim
     bwd = win + 2 * c.n_real_rows * c.head_dim + ape + 4 * c.n_tokens * C + ape
     return fwd, bwd
 

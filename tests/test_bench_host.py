@@ -60,3 +60,66 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+# ------------------------------------------------- algorithmic bytes (roofline)
+
+def _shape_case(ratio, coff, head_dim, lens, capacity=None, extra_rows=0, leading=0):
+    sys.path.insert(0, ROOT)
+    import csa_workloads as w
+    cu, cc = w.offsets(lens, ratio, leading)
+    cap = int(cc[-1]) + extra_rows if capacity is None else capacity
+    return w.Case("shape", ratio, coff, head_dim, list(lens), cap, int(cu[-1]), cu, cc, None, None, None, None)
+
+
+def _window_term_by_enumeration(c, rows):
+    """Distinct (token, half) slots the given rows read, from the oracle's gather
+    window map, as bytes of kv + score (2 bf16 per column)."""
+    import numpy as np
+    from oracle import gather
+    token, half, _, valid, real = gather.window_index(c.cu_seqlens, c.cu_seqlens_comp, c.ratio, c.coff,
+                                                      c.capacity)
+    sel = valid & (real if rows == "real" else np.ones_like(real))[:, None]
+    h = np.broadcast_to(half[None, :], token.shape)
+    return len(np.unique(token[sel] * 2 + h[sel])) * c.head_dim * 4
+
+
+def _check_bytes(c):
+    sys.path.insert(0, ROOT)
+    import bench
+    fwd, bwd = bench.algorithmic_bytes(c)
+    C = c.coff * c.head_dim
+    ape = 4 * c.ratio * C
+    assert fwd == _window_term_by_enumeration(c, "all") + ape + 2 * c.capacity * c.head_dim
+    assert bwd == (_window_term_by_enumeration(c, "real") + 2 * c.n_real_rows * c.head_dim + ape
+                   + 4 * c.n_tokens * C + ape)
+
+
+def test_algorithmic_bytes_of_every_workload_match_the_window_map():
+    """The roofline's numerator: each consumed kv / score slot once (forward: every
+    row, padding rows included; backward: real rows), counted against a brute-force
+    enumeration of the oracle's window map on the benchmark layouts."""
+    sys.path.insert(0, ROOT)
+    import csa_workloads as w
+    for name, spec in w.SPECS.items():
+        kw = spec(0)
+        c = _shape_case(kw["ratio"], kw["coff"], kw["head_dim"], kw["seqlens"], capacity=kw.get("capacity"),
+                        extra_rows=kw.get("extra_rows", 0))
+        _check_bytes(c)
+
+
+def test_algorithmic_bytes_on_ragged_layouts():
+    """Short and empty segments, tails, leading tokens and padding rows whose tokens
+    [0, ratio) no real row reads."""
+    import numpy as np
+    rng = np.random.default_rng(0)
+    n = 0
+    while n < 400:
+        ratio = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+        lens = [int(x) for x in rng.integers(0, 4 * ratio + 2, int(rng.integers(1, 5)))]
+        c = _shape_case(ratio, int(rng.integers(1, 3)), 8, lens, extra_rows=int(rng.choice([0, 1, 3])),
+                        leading=int(rng.choice([0, 0, 2])))
+        if c.capacity == 0 or c.n_tokens < ratio:
+            continue
+        _check_bytes(c)
+        n += 1
