@@ -12,7 +12,9 @@ alone the same way (K calls back to back).  `e2e` is the same metric
 through the C ABI with pinned host buffers: host-to-device copies of the
 inputs, forward, backward and device-to-host copies of all outputs inside the
 timed region; consecutive steps overlap their copies and compute on three streams
-(two buffer sets), as a data pipeline would.
+(two buffer sets), as a data pipeline would.  The default run also times the
+other packs the throughput target is stated on (ragged ratio 4, ratio 128 with the
+own-block window, the one-segment stress pack) the same way, under `workloads`.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl ours|reference]
 
@@ -41,6 +43,10 @@ import csa_workloads as w  # noqa: E402
 
 METRIC = "CSA compressor fwd/bwd tokens/s and achieved HBM GB/s (% of GB300 peak)"
 INPUT_SETS = 3  # rotating copies of the inputs (3 x 136 MB for the default pack; L2 is 126 MB)
+DEFAULT_WORKLOAD = "r4c2d512_8x4096"
+# the other packs the throughput target is stated on (ragged ratio 4, ratio 128,
+# and the one-segment stress pack at unit scale), timed in the default run
+EXTRA_WORKLOADS = ("r4c2d512_ragged64", "r128c1d512_4x32768", "stress_unit")
 
 
 def parse_args():
@@ -49,7 +55,9 @@ def parse_args():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="r4c2d512_8x4096", choices=sorted(w.WORKLOADS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(w.WORKLOADS))
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip timing the other workloads (default run only)")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target CPU time of the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -184,6 +192,65 @@ def recorded_traffic(kernel):
     return rec["bytes_per_launch"] if h.hexdigest() == rec["sha256"] else None
 
 
+class Resident:
+    """A workload resident on the device: INPUT_SETS copies of the inputs used in
+    rotation (kernel call k reads set k % INPUT_SETS, last touched three calls
+    earlier, with more than L2's worth of other traffic in between, so every call
+    streams its inputs from HBM), and the outputs."""
+
+    def __init__(self, csa, c, dev, stream, world):
+        import torch
+        self.csa, self.c, self.stream, self.world = csa, c, stream, world
+        C = c.coff * c.head_dim
+
+        def up(a):
+            a = np.ascontiguousarray(a)
+            return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+        kv0, sc0, g0 = up(c.kv), up(c.score), up(c.grad_out)
+        self.sets = [(kv0, sc0, g0)] + [(kv0.clone(), sc0.clone(), g0.clone()) for _ in range(INPUT_SETS - 1)]
+        self.ape, self.cu, self.cc = up(c.ape), up(c.cu_seqlens), up(c.cu_seqlens_comp)
+        self.out = torch.empty((c.capacity, c.head_dim), dtype=torch.int16, device=dev)
+        self.dkv = torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev)
+        self.dsc = torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev)
+        self.dape = torch.empty((c.ratio, C), dtype=torch.float32, device=dev)
+
+    def fwd(self, k):
+        c = self.c
+        kv, sc, _ = self.sets[k % INPUT_SETS]
+        self.csa.csa_compress_fwd(kv, sc, self.ape, self.cu, self.cc, c.n_seg, c.ratio, c.coff, c.head_dim,
+                                  c.capacity, self.out, self.stream)
+
+    def bwd(self, k):
+        c = self.c
+        kv, sc, g = self.sets[k % INPUT_SETS]
+        self.csa.csa_compress_bwd(kv, sc, self.ape, self.cu, self.cc, c.n_seg, c.ratio, c.coff, c.head_dim,
+                                  c.capacity, c.n_tokens, g, self.dkv, self.dsc, self.dape, self.stream)
+
+    def step(self, i):
+        self.fwd(2 * i)
+        self.bwd(2 * i + 1)
+
+    def region(self, fn, k):
+        """k calls fn(0..k-1) back to back between two events: mean ms per call."""
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0.record(self.stream)
+        for i in range(k):
+            fn(i)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        if self.world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / k
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import sparse_attention_kv_csa_gb300 as csa
@@ -191,54 +258,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     c = w.WORKLOADS[args.workload](seed=rank)
-    C = c.coff * c.head_dim
-
-    def up(a):
-        a = np.ascontiguousarray(a)
-        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
-
-    # INPUT_SETS copies of the inputs, used in rotation: kernel call k reads set
-    # k % INPUT_SETS, last touched three calls earlier, with more than L2's worth
-    # of other traffic in between, so every call streams its inputs from HBM.
-    kv0, sc0, g0 = up(c.kv), up(c.score), up(c.grad_out)
-    sets = [(kv0, sc0, g0)] + [(kv0.clone(), sc0.clone(), g0.clone()) for _ in range(INPUT_SETS - 1)]
-    ape, cu, cc = up(c.ape), up(c.cu_seqlens), up(c.cu_seqlens_comp)
-    out = torch.empty((c.capacity, c.head_dim), dtype=torch.int16, device=dev)
-    dkv = torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev)
-    dsc = torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev)
-    dape = torch.empty((c.ratio, C), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
-
-    def fwd(k):
-        kv, sc, _ = sets[k % INPUT_SETS]
-        csa.csa_compress_fwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity, out, stream)
-
-    def bwd(k):
-        kv, sc, g = sets[k % INPUT_SETS]
-        csa.csa_compress_bwd(kv, sc, ape, cu, cc, c.n_seg, c.ratio, c.coff, c.head_dim, c.capacity,
-                             c.n_tokens, g, dkv, dsc, dape, stream)
-
-    def step(i):
-        fwd(2 * i)
-        bwd(2 * i + 1)
-
-    def region(fn, k):
-        """k calls fn(0..k-1) back to back between two events: mean ms per call."""
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for i in range(k):
-            fn(i)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / k
+    r = Resident(csa, c, dev, stream, world)
 
     sampler = ClockSampler(local_rank) if rank == 0 and not args.no_clocks else None
     if sampler:
@@ -248,20 +269,56 @@ def run_ours(args, rank, world, local_rank):
     t_end = time.time() + args.min_warmup_seconds
     n = 0
     while n < args.warmup or time.time() < t_end:
-        step(n)
+        r.step(n)
         n += 1
         if n % 10 == 0:
             torch.cuda.synchronize()
     # the timed region: K whole steps (forward + backward)
-    ms_step = region(step, args.steps)
+    ms_step = r.region(r.step, args.steps)
     # each pass alone, K calls back to back (its average launch duration)
-    ms_fwd = region(lambda i: fwd(i), args.steps)
-    ms_bwd = region(lambda i: bwd(i), args.steps)
-    clocks = sampler.stop() if sampler else None
+    ms_fwd = r.region(r.fwd, args.steps)
+    ms_bwd = r.region(r.bwd, args.steps)
     ms_step, ms_fwd, ms_bwd = max_over_ranks([ms_step, ms_fwd, ms_bwd])
+    del r
+    extra = {}
+    if args.workload == DEFAULT_WORKLOAD and not args.no_extra:
+        extra = run_extra(args, csa, dev, stream, rank, world)
+    clocks = sampler.stop() if sampler else None
 
     e2e = None if args.no_e2e else run_e2e(args, c, csa, dev, stream, world)
-    return c, ms_step, ms_fwd, ms_bwd, clocks, e2e
+    return c, ms_step, ms_fwd, ms_bwd, clocks, e2e, extra
+
+
+def run_extra(args, csa, dev, stream, rank, world):
+    """The other workloads the throughput target names, each timed like the main
+    one (rotating input sets, K calls of each pass back to back after a warm-up):
+    per pass the mean time per call, tokens/s and algorithmic GB/s against the
+    measured HBM peak."""
+    import torch
+    peak, _ = measured_peak()
+    res = {}
+    for name in EXTRA_WORKLOADS:
+        c = w.WORKLOADS[name](seed=rank)
+        r = Resident(csa, c, dev, stream, world)
+        for i in range(max(3, args.warmup)):
+            r.step(i)
+        ms_fwd = r.region(r.fwd, args.steps)
+        ms_bwd = r.region(r.bwd, args.steps)
+        ms_fwd, ms_bwd = max_over_ranks([ms_fwd, ms_bwd])
+        fb, bb = algorithmic_bytes(c)
+        gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+        res[name] = {
+            "ratio": c.ratio, "coff": c.coff, "head_dim": c.head_dim, "segments": len(c.seqlens),
+            "tokens": c.n_tokens, "rows": c.n_real_rows, "capacity": c.capacity,
+            "fwd": {"us": ms_fwd * 1e3, "tokens_per_s": world * c.n_tokens / (ms_fwd * 1e-3), "bytes": fb,
+                    "gbs": gbs(fb, ms_fwd), "frac": gbs(fb, ms_fwd) / peak},
+            "bwd": {"us": ms_bwd * 1e3, "tokens_per_s": world * c.n_tokens / (ms_bwd * 1e-3), "bytes": bb,
+                    "gbs": gbs(bb, ms_bwd), "frac": gbs(bb, ms_bwd) / peak},
+        }
+        del r, c
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(args, c, csa, dev, stream, world):
@@ -445,7 +502,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    c, ms_step, ms_fwd, ms_bwd, clocks, e2e = run_ours(args, rank, world, local_rank)
+    c, ms_step, ms_fwd, ms_bwd, clocks, e2e, extra = run_ours(args, rank, world, local_rank)
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -485,6 +542,8 @@ def main():
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
+    if extra:
+        line["workloads"] = extra
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:

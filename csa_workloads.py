@@ -20,7 +20,9 @@ ape ~ N(0, 0.25^2) fp32.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 
 import numpy as np
 
@@ -54,26 +56,36 @@ def uniform01(seed: int, stream: int, n: int, offset: int = 0) -> np.ndarray:
     return ((z >> np.uint64(11)).astype(np.float64) + 0.5) * (1.0 / 9007199254740992.0)
 
 
-def normal(seed: int, stream: int, n: int, sigma: float = 1.0, chunk: int = 1 << 20) -> np.ndarray:
+def normal(seed: int, stream: int, n: int, sigma: float = 1.0, chunk: int = 1 << 18) -> np.ndarray:
     """n N(0, sigma^2) doubles by Box-Muller: draws 2i and 2i+1 of the stream give
-    normals 2i (cosine) and 2i+1 (sine).  Computed in chunks to stay cache-sized."""
+    normals 2i (cosine) and 2i+1 (sine).  Computed in cache-sized chunks; the
+    generator is counter-based, so the chunks are independent and run on a pool of
+    threads (numpy releases the interpreter lock in its array operations), with the
+    same values as a sequential pass."""
     m = (n + 1) // 2
     z = np.empty(2 * m, dtype=np.float64)
-    for s0 in range(0, m, chunk):
+
+    def one(s0):
         s1 = min(m, s0 + chunk)
         u = uniform01(seed, stream, 2 * (s1 - s0), offset=2 * s0)
         rad = np.sqrt(-2.0 * np.log(u[0::2]))
         ang = 2.0 * np.pi * u[1::2]
         z[2 * s0:2 * s1:2] = rad * np.cos(ang)
         z[2 * s0 + 1:2 * s1:2] = rad * np.sin(ang)
+
+    starts = range(0, m, chunk)
+    if len(starts) > 1:
+        with concurrent.futures.ThreadPoolExecutor(min(len(starts), os.cpu_count() or 1, 32)) as ex:
+            list(ex.map(one, starts))
+    elif m:
+        one(0)
     z = z[:n]
     if sigma != 1.0:
         z *= sigma
     return z
 
 
-def to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round float values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
+def _bf16_chunk(x: np.ndarray) -> np.ndarray:
     f = np.array(x, dtype=np.float32, copy=True, order="C")
     u = f.view(np.uint32)
     nan = np.isnan(f)
@@ -85,6 +97,23 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     r = u.astype(np.uint16)
     r[nan] = 0x7FC0
     return r
+
+
+def to_bf16_bits(x: np.ndarray, chunk: int = 1 << 20) -> np.ndarray:
+    """Round float values to bf16 (nearest, ties to even); returns uint16 bit patterns.
+    Elementwise, so large arrays are cut into chunks converted on a pool of threads."""
+    x = np.asarray(x)
+    if x.size <= chunk:
+        return _bf16_chunk(x)
+    flat = x.reshape(-1)
+    out = np.empty(flat.size, dtype=np.uint16)
+
+    def one(s0):
+        out[s0:s0 + chunk] = _bf16_chunk(flat[s0:s0 + chunk])
+
+    with concurrent.futures.ThreadPoolExecutor(min(os.cpu_count() or 1, 32)) as ex:
+        list(ex.map(one, range(0, flat.size, chunk)))
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:

@@ -118,7 +118,8 @@ CSA_API int csa_compress_fwd(const void *kv, const void *score, const float *ape
  *                shorter than ratio, tokens outside the segments);
  *   dape         overwritten (not accumulated) with the sum over real rows, formed
  *                as fixed-order partial sums: no atomics, bitwise reproducible
- *                run to run.
+ *                run to run.  The grouping of that sum for a given shape and
+ *                device is reported by csa_grad_ape_order (below).
  * grad_out rows at or past cu_seqlens_comp[n_seg] are ignored.
  * Scratch: grad_ape partials (a few MB at most) come from a library-owned,
  * stream-ordered memory pool on the current device, allocated and released in
@@ -155,7 +156,12 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * call writes all it reads, so nothing needs clearing, but calls that overlap on
  * the GPU (different streams or host threads) race: order them.  The first call
  * on a device (with that device current) looks up the array's device address;
- * make that first call before any stream capture.
+ * make that first call before any stream capture.  A first call whose set-up
+ * fails returns CSA_ERR_CUDA and leaves nothing behind: the next call tries the
+ * set-up again.  Bounded device waits that expire in this call's kernels are
+ * recorded in the same per-device status word as those of every other call, so
+ * csa_device_status() reports them (CSA_ERR_DEVICE_TIMEOUT).  The grad_ape
+ * grouping is csa_grad_ape_order's for every ratio but 128.
  */
 CSA_API int csa_compress_bwd_noalloc(const void *kv, const void *score, const float *ape,
                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_comp, int32_t n_seg,
@@ -180,13 +186,68 @@ CSA_API const char *csa_status_string(int status);
 CSA_API const char *csa_last_error_message(void);
 
 /*
+ * How the backward groups the grad_ape sum (the pages fix only that grad_ape is
+ * the sum over real rows of ds and, in this library, that it is deterministic; the
+ * grouping is the implementation's choice and depends on the shape and the
+ * device).  Host-side: launches nothing, reads no device memory and allocates
+ * nothing, but queries the current device's SM count and the kernels' occupancy.
+ *
+ * kind == CSA_GRAD_APE_ROW_BLOCKS (every ratio but 128), with R = the real row
+ * count (cu_seqlens_comp[n_seg], at most capacity):
+ *   1. Row blocks.  strided != 0: block b (0 <= b < blocks) takes the rows
+ *      b, b + blocks, b + 2*blocks, ... below R.  strided == 0: block b takes the
+ *      rows [b*rows_per_block, (b+1)*rows_per_block) below R.
+ *   2. Lanes.  The i-th row of a block (i = 0, 1, ... in ascending row order) goes
+ *      to the block's lane i % lanes.  Each lane sums, in fp32 from +0, the ds of
+ *      its rows in ascending row order: one leaf per (block, lane).
+ *   3. Partials.  Partial q takes the blocks [q*cluster, (q+1)*cluster).  flat != 0:
+ *      the partial is the left-to-right fp32 sum of its leaves in ascending
+ *      (block, lane) order, starting with the first leaf itself.  flat == 0: each
+ *      block first sums its lanes that way, then the partial sums its blocks that
+ *      way.
+ *   4. Final sum.  The partials are cut into final_ranges (32) contiguous ranges,
+ *      range t = [t*partials/32, (t+1)*partials/32) in integer division, each summed
+ *      from +0 in ascending order; then the 32 range sums are added in pairs
+ *      (t, t^1), then (t, t^2), (t, t^4), (t, t^8), (t, t^16): a balanced binary
+ *      tree over the ranges in order.
+ * kind == CSA_GRAD_APE_CHUNKED (ratio 128): every sum of the ratio-128 kernels is
+ * taken in fixed chunks (section ratio=128 of the page); grad_ape is deterministic
+ * but has no bitwise contract.  blocks, partials and cluster describe the grid.
+ *
+ * Errors: those of csa_check_support for the shape, CSA_ERR_INVALID_VALUE for a
+ * NULL out, CSA_ERR_CUDA if the device cannot be queried.
+ */
+typedef enum csa_grad_ape_kind {
+    CSA_GRAD_APE_ROW_BLOCKS = 0,
+    CSA_GRAD_APE_CHUNKED = 1
+} csa_grad_ape_kind;
+
+typedef struct csa_grad_ape_grouping {
+    int32_t kind;            /* csa_grad_ape_kind                                       */
+    int32_t strided;         /* rows of block b: strided (b + i*blocks) or contiguous   */
+    int32_t blocks;          /* row blocks                                              */
+    int32_t rows_per_block;  /* contiguous row blocks: rows per block                   */
+    int32_t lanes;           /* lanes per block                                         */
+    int32_t cluster;         /* row blocks per partial                                  */
+    int32_t flat;            /* 1: a partial sums its (block, lane) leaves in one pass  */
+    int32_t partials;        /* blocks / cluster                                        */
+    int32_t final_ranges;    /* 32                                                      */
+} csa_grad_ape_grouping;
+
+CSA_API int csa_grad_ape_order(int32_t ratio, int32_t coff, int32_t head_dim, int32_t capacity,
+                               csa_grad_ape_grouping *out);
+
+/*
  * Device-side status of the current device, for diagnostics.  Kernels that wait
  * on shared-memory barriers (the bulk-copy pipelines) bound every wait in time;
  * on expiry they record a code in a per-device status word, stop, and exit
  * normally, so that a wait that can never complete gives an error instead of a
- * hung GPU.  This call SYNCHRONISES with the device (it reads the word back),
- * returns CSA_OK if no kernel recorded anything and CSA_ERR_DEVICE_TIMEOUT
- * otherwise; clear != 0 resets the word.  Not meant for the hot path.
+ * hung GPU.  One word per device serves every entry point (csa_compress_fwd,
+ * csa_compress_bwd, csa_compress_bwd_noalloc, csa_selftest_bounded_wait); it is
+ * part of the library's device code, so reading it allocates nothing.  This call
+ * SYNCHRONISES with the device (it reads the word back), returns CSA_OK if no
+ * kernel recorded anything and CSA_ERR_DEVICE_TIMEOUT otherwise; clear != 0
+ * resets the word.  Not meant for the hot path.
  */
 CSA_API int csa_device_status(int clear);
 

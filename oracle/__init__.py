@@ -57,8 +57,9 @@ def _bind(lib):
     lib.csa_oracle_bwd_f32.argtypes = common + [i64, P, P, P, P]
     lib.csa_oracle_bwd_f64.argtypes = common + [i64, P, P, P, P, P]
     lib.csa_oracle_consumers.argtypes = [P, P, i32, i32, i32, i32, i32, i64, P]
+    lib.csa_oracle_dape_leaves_f32.argtypes = common + [P, P, i32, P]
     for f in ("csa_oracle_fwd_f32", "csa_oracle_fwd_f64", "csa_oracle_bwd_f32",
-              "csa_oracle_bwd_f64", "csa_oracle_consumers"):
+              "csa_oracle_bwd_f64", "csa_oracle_consumers", "csa_oracle_dape_leaves_f32"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -172,6 +173,84 @@ def bwd_f64(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim, 
                                     _ptr(dabs) if with_abs else None)
     assert rc == 0, rc
     return (dkv, ds, dape, dabs) if with_abs else (dkv, ds, dape)
+
+
+def dape_leaves_f32(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim, capacity,
+                    grad_out, leaf_of_row, n_leaves):
+    """[n_leaves, ratio, coff*head_dim] fp32: leaf i = the fp32 sum, from +0 in ascending
+    row order, of the ds of the real rows r with leaf_of_row[r] == i."""
+    keep, a = _args(kv, score, ape, cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim, capacity)
+    g = _c(grad_out, np.uint16)
+    lor = _c(leaf_of_row, np.int32)
+    assert lor.shape == (capacity,)
+    leaves = np.empty((n_leaves, ratio, coff * head_dim), dtype=np.float32)
+    rc = _load().csa_oracle_dape_leaves_f32(*a, _ptr(g), _ptr(lor), n_leaves, _ptr(leaves))
+    assert rc == 0, rc
+    return leaves
+
+
+def leaf_of_row(grouping, capacity, n_real_rows):
+    """Row -> leaf map of a row-block grouping (the rules stated for csa_grad_ape_order
+    in include/csa.h): rows of block b strided (b, b + blocks, ...) or contiguous
+    ([b * rows_per_block, ...)), the i-th row of a block in lane i % lanes, leaf
+    b * lanes + lane.  Padding rows (>= n_real_rows) map to -1."""
+    B, L = grouping["blocks"], grouping["lanes"]
+    leaf = np.full(capacity, -1, dtype=np.int32)
+    for r in range(min(n_real_rows, capacity)):
+        if grouping["strided"]:
+            b, i = r % B, r // B
+        else:
+            b = r // grouping["rows_per_block"]
+            i = r - b * grouping["rows_per_block"]
+        assert b < B, (r, b, B)
+        leaf[r] = b * L + i % L
+    return leaf
+
+
+def combine_leaves(leaves, grouping):
+    """grad_ape from the leaves [blocks * lanes, ...] of a row-block grouping, in fp32,
+    following the stated combination: leaves into partials (one left-to-right pass
+    over (block, lane) when flat, else lanes within each block and then blocks),
+    then the partials cut into 32 contiguous ranges summed from +0, then the range
+    sums added in pairs (t, t ^ m) for m = 1, 2, 4, 8, 16."""
+    B, L, CL = grouping["blocks"], grouping["lanes"], grouping["cluster"]
+    P = B // CL
+    assert P == grouping["partials"] and grouping["final_ranges"] == 32
+    assert leaves.shape[0] == B * L and leaves.dtype == np.float32
+
+    def fold(xs):
+        s = xs[0].copy()
+        for v in xs[1:]:
+            s = s + v
+        return s
+
+    partials = []
+    for q in range(P):
+        blocks = range(q * CL, (q + 1) * CL)
+        if grouping["flat"]:
+            partials.append(fold([leaves[b * L + l] for b in blocks for l in range(L)]))
+        else:
+            partials.append(fold([fold([leaves[b * L + l] for l in range(L)]) for b in blocks]))
+    sub = []
+    for t in range(32):
+        s = np.zeros(leaves.shape[1:], dtype=np.float32)
+        for b in range(t * P // 32, (t + 1) * P // 32):
+            s = s + partials[b]
+        sub.append(s)
+    m = 1
+    while m < 32:
+        sub = [sub[t] + sub[t ^ m] for t in range(32)]
+        m *= 2
+    return sub[0]
+
+
+def case_dape_grouped_f32(c, grouping):
+    """The fp32 grad_ape of a csa_workloads.Case summed in a row-block grouping."""
+    assert grouping["kind"] == "row_blocks"
+    lor = leaf_of_row(grouping, c.capacity, c.n_real_rows)
+    leaves = dape_leaves_f32(c.kv, c.score, c.ape, c.cu_seqlens, c.cu_seqlens_comp, c.ratio, c.coff,
+                             c.head_dim, c.capacity, c.grad_out, lor, grouping["blocks"] * grouping["lanes"])
+    return combine_leaves(leaves, grouping)
 
 
 def consumers(cu_seqlens, cu_seqlens_comp, ratio, coff, head_dim, capacity, n_tokens):

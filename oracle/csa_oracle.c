@@ -435,3 +435,60 @@ int csa_oracle_consumers(const int32_t *cu_seqlens, const int32_t *cu_seqlens_co
     }
     return 0;
 }
+
+/* ------------------------------------------- grad_ape in a stated grouping */
+
+/* The pages fix grad_ape only as a sum over the real rows (Semantics: the chain
+ * rule through the pooling) and ask that it be deterministic (Numerics).  How the
+ * rows are grouped for that sum is the implementation's choice.  This function
+ * evaluates the first level of any grouping plainly: leaf_of_row[r] names the
+ * leaf (0 <= leaf < n_leaves) that real row r belongs to, and each leaf is the fp32
+ * sum, from +0 in ascending row order, of the ds values of its rows -- the same ds
+ * as csa_oracle_bwd_f32 computes.  leaves is [n_leaves][ratio][coff*head_dim].
+ * Every real row must name a leaf (the sum takes each row exactly once); rows at
+ * or past cu_seqlens_comp[n_seg] are padding rows and are not read.  How leaves
+ * combine into grad_ape is left to the caller. */
+int csa_oracle_dape_leaves_f32(const uint16_t *kv, const uint16_t *score, const float *ape,
+                               const int32_t *cu_seqlens, const int32_t *cu_seqlens_comp,
+                               int32_t n_seg, int32_t ratio, int32_t coff, int32_t head_dim,
+                               int32_t capacity, const uint16_t *grad_out,
+                               const int32_t *leaf_of_row, int32_t n_leaves, float *leaves)
+{
+    if (check_args(n_seg, ratio, coff, head_dim, capacity) || n_leaves < 1)
+        return -1;
+    const int32_t W = coff * ratio;
+    const int64_t C = (int64_t)coff * head_dim;
+    for (int64_t i = 0; i < (int64_t)n_leaves * ratio * C; ++i)
+        leaves[i] = 0.0f;
+    float *e = (float *)malloc(sizeof(float) * (size_t)W);
+    if (!e)
+        return -2;
+    for (int64_t r = 0; r < capacity; ++r) {
+        row_info ri = row_of(r, cu_seqlens, cu_seqlens_comp, n_seg, ratio);
+        if (!ri.real)
+            continue;
+        const int32_t leaf = leaf_of_row[r];
+        if (leaf < 0 || leaf >= n_leaves) {
+            free(e);
+            return -3;
+        }
+        float *acc = leaves + (int64_t)leaf * ratio * C;
+        for (int64_t j = 0; j < head_dim; ++j) {
+            float inv;
+            float o = pool_f32(kv, score, ape, &ri, j, ratio, coff, head_dim, e, &inv);
+            float g = bf16_to_f32(grad_out[r * head_dim + j]);
+            float go = g * o;
+            for (int32_t k = 0; k < W; ++k) {
+                slot sl = slot_of(&ri, k, j, ratio, coff, head_dim);
+                if (!sl.valid)
+                    continue;
+                float p = e[k] * inv;
+                float v = bf16_to_f32(kv[sl.token * C + sl.col]);
+                float ds_k = p * (g * v - go);
+                acc[sl.ape_row * C + sl.col] += ds_k;
+            }
+        }
+    }
+    free(e);
+    return 0;
+}

@@ -13,6 +13,8 @@ The C entry points keep their names here:
                      coff, head_dim, capacity, n_tokens, grad_out, dkv, dscore,
                      dape, stream=None)
     csa_check_support(ratio, coff, head_dim, n_tokens, capacity) -> int status
+    csa_grad_ape_order(ratio, coff, head_dim, capacity) -> dict (the backward's
+                     grad_ape grouping on the current device; host-side)
 Tensor arguments may be torch tensors (their data_ptr() is passed) or integer
 device addresses.  bf16 tensors may be torch.bfloat16 or any 16-bit dtype
 holding bf16 bit patterns.  ``stream`` is a torch.cuda.Stream, a raw
@@ -31,7 +33,7 @@ from . import _build
 __all__ = [
     "csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support", "csa_status_string",
     "csa_last_error_message", "csa_version", "csa_device_status", "csa_selftest_bounded_wait",
-    "csa_selftest_reciprocal", "CSAError", "compress_forward", "compress_backward",
+    "csa_selftest_reciprocal", "csa_grad_ape_order", "CSAError", "compress_forward", "compress_backward",
     "library_path", "STATUS",
 ]
 
@@ -47,6 +49,11 @@ class CSAError(RuntimeError):
         self.status = status
 
 
+class _Grouping(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("kind", "strided", "blocks", "rows_per_block", "lanes", "cluster",
+                                               "flat", "partials", "final_ranges")]
+
+
 def _load():
     path = _build.build()  # no-op when up to date
     lib = ctypes.CDLL(path)
@@ -59,12 +66,14 @@ def _load():
     lib.csa_device_status.argtypes = [ctypes.c_int]
     lib.csa_selftest_bounded_wait.argtypes = [i64, P]
     lib.csa_selftest_reciprocal.argtypes = [P, P, i64, P]
+    lib.csa_grad_ape_order.argtypes = [i32, i32, i32, i32, ctypes.POINTER(_Grouping)]
     lib.csa_status_string.argtypes = [ctypes.c_int]
     lib.csa_status_string.restype = ctypes.c_char_p
     lib.csa_last_error_message.argtypes = []
     lib.csa_last_error_message.restype = ctypes.c_char_p
     for f in ("csa_compress_fwd", "csa_compress_bwd", "csa_compress_bwd_noalloc", "csa_check_support",
-              "csa_version", "csa_device_status", "csa_selftest_bounded_wait", "csa_selftest_reciprocal"):
+              "csa_version", "csa_device_status", "csa_selftest_bounded_wait", "csa_selftest_reciprocal",
+              "csa_grad_ape_order"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -127,6 +136,17 @@ def csa_selftest_reciprocal(d, out, n: int, stream=None) -> None:
 
 def csa_check_support(ratio, coff, head_dim, n_tokens, capacity) -> int:
     return _lib.csa_check_support(ratio, coff, head_dim, n_tokens, capacity)
+
+
+def csa_grad_ape_order(ratio, coff, head_dim, capacity) -> dict:
+    """How the backward groups the grad_ape sum for this shape on the current device
+    (see csa.h): kind ("row_blocks" or "chunked"), strided, blocks, rows_per_block,
+    lanes, cluster, flat, partials, final_ranges."""
+    g = _Grouping()
+    _check(_lib.csa_grad_ape_order(ratio, coff, head_dim, capacity, ctypes.byref(g)))
+    d = {n: int(getattr(g, n)) for n, _ in _Grouping._fields_}
+    d["kind"] = {0: "row_blocks", 1: "chunked"}[d["kind"]]
+    return d
 
 
 def csa_compress_fwd(kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,

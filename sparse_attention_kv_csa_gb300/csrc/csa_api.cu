@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -42,15 +43,17 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 constexpr int64_t kInt32Limit = int64_t(1) << 31;
 constexpr int kMaxDevices = 64;
 
-// Per-device facts and the workspace pool, created on first use on that device.
+// Per-device facts and the workspace pool, created on first use on that device.  A
+// set-up that fails (a transient runtime error, a first call made during stream
+// capture) is not remembered: the next call on that device tries again.
 struct DeviceState {
-    std::once_flag once;
-    cudaError_t init_err = cudaSuccess;
+    std::atomic<bool> ready{false};
     int num_sms = 0;
     cudaMemPool_t pool = nullptr;
     unsigned *status = nullptr;  // device status word written by bounded waits
 };
 DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mu;
 
 cudaError_t device_state(DeviceState **out)
 {
@@ -61,9 +64,16 @@ cudaError_t device_state(DeviceState **out)
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
     DeviceState &d = g_dev[dev];
-    std::call_once(d.once, [&d, dev]() {
-        cudaError_t err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
-        if (err == cudaSuccess) {
+    if (d.ready.load(std::memory_order_acquire)) {
+        *out = &d;
+        return cudaSuccess;
+    }
+    std::lock_guard<std::mutex> g(g_dev_mu);
+    if (!d.ready.load(std::memory_order_relaxed)) {
+        e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = csa::status_word(&d.status);
+        if (e == cudaSuccess && !d.pool) {
             // A pool of its own, so that the workspace stays cached between calls
             // without changing the device's default pool.
             cudaMemPoolProps props;
@@ -72,20 +82,23 @@ cudaError_t device_state(DeviceState **out)
             props.handleTypes = cudaMemHandleTypeNone;
             props.location.type = cudaMemLocationTypeDevice;
             props.location.id = dev;
-            err = cudaMemPoolCreate(&d.pool, &props);
-            if (err == cudaSuccess) {
+            cudaMemPool_t pool = nullptr;
+            e = cudaMemPoolCreate(&pool, &props);
+            if (e == cudaSuccess) {
                 uint64_t keep = 256ull << 20;
-                err = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+                e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+                if (e == cudaSuccess)
+                    d.pool = pool;
+                else
+                    cudaMemPoolDestroy(pool);
             }
-            if (err == cudaSuccess)
-                err = cudaMalloc(reinterpret_cast<void **>(&d.status), 256);
-            if (err == cudaSuccess)
-                err = cudaMemset(d.status, 0, 256);
         }
-        d.init_err = err;
-    });
+        if (e != cudaSuccess)
+            return e;
+        d.ready.store(true, std::memory_order_release);
+    }
     *out = &d;
-    return d.init_err;
+    return cudaSuccess;
 }
 
 int check_common(int32_t n_seg, int32_t ratio, int32_t coff, int32_t head_dim, int32_t capacity)
@@ -307,6 +320,70 @@ cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int b
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The status word of the bounded waits, one per device: a word of this module's
+// device memory, so that neither entry point has to allocate it.
+static __device__ __align__(256) unsigned g_status_word[64];
+
+cudaError_t status_word(unsigned **word)
+{
+    static std::mutex mu;
+    static unsigned *addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kMaxDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(mu);
+    if (!addr[dev]) {
+        // The symbol's name is a host-side stand-in: ask for its address on this
+        // (current) device.
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&addr[dev]), g_status_word);
+        if (e != cudaSuccess) {
+            addr[dev] = nullptr;
+            return e;
+        }
+    }
+    *word = addr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t plan_bwd(int ratio, int coff, int head_dim, int capacity, int num_sms, BwdPlan *out)
+{
+    BwdPlan b{};
+    cudaError_t e = cudaSuccess;
+    if (r128_supported(ratio, coff, head_dim)) {
+        b.family = kBwdR128;
+        e = r128_bwd_partials(coff, head_dim, capacity, &b.r128_partials, &b.r128_blocks);
+        b.floats = (int64_t)b.r128_partials * ratio * coff * head_dim;
+    } else if (ratio != 4) {
+        b.family = kBwdGeneric;
+        e = plan_generic(ratio, coff, head_dim, capacity, num_sms, &b.gp);
+        b.floats = b.gp.partial_floats;
+    } else if (stream_supported(ratio, coff, head_dim)) {
+        b.family = kBwdStream;
+        b.sp = plan_stream(true, ratio, coff, head_dim, capacity, num_sms);
+        e = stream_bwd_blocks(ratio, coff, b.sp, capacity, &b.stream_blocks);
+        b.floats = (int64_t)stream_bwd_partials(b.sp, capacity) * ratio * coff * head_dim;
+    } else {
+        b.family = kBwdSmall;
+        b.pl = plan_bwd_small(ratio, coff, head_dim, capacity, num_sms);
+        b.floats = b.pl.partial_floats;
+    }
+    *out = b;
+    return e;
+}
+
+cudaError_t launch_bwd(const BwdParams &p, const BwdPlan &b, float *partial, unsigned *status, cudaStream_t st)
+{
+    switch (b.family) {
+    case kBwdR128: return launch_bwd_r128(p, partial, b.r128_blocks, status, st);
+    case kBwdGeneric: return launch_bwd_generic(p, b.gp, partial, status, st);
+    case kBwdStream: return launch_bwd_stream(p, b.sp, partial, status, st);
+    default: return launch_bwd_small(p, b.pl, partial, st);
+    }
+}
+
 int fail_status(int status, const char *fmt, ...)
 {
     va_list ap;
@@ -407,44 +484,15 @@ int csa_compress_bwd(const void *kv, const void *score, const float *ape, const 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
-    const bool r128 = csa::r128_supported(ratio, coff, head_dim);
-    const bool generic = !r128 && ratio != 4;
-    const bool streamed = !r128 && !generic && csa::stream_supported(ratio, coff, head_dim);
-    csa::StreamPlan sp{};
-    csa::SmallBwdPlan pl{};
-    csa::GenericPlan gp{};
-    int64_t floats = 0;
-    int r128_blocks = 0;
-    if (r128) {
-        int partials = 0;
-        e = csa::r128_bwd_partials(coff, head_dim, capacity, &partials, &r128_blocks);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "backward plan");
-        floats = (int64_t)partials * ratio * coff * head_dim;
-    } else if (generic) {
-        e = csa::plan_generic(ratio, coff, head_dim, capacity, ds->num_sms, &gp);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "backward plan");
-        floats = gp.partial_floats;
-    } else if (streamed) {
-        sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, ds->num_sms);
-        floats = (int64_t)csa::stream_bwd_partials(sp, capacity) * ratio * coff * head_dim;
-    } else {
-        pl = csa::plan_bwd_small(ratio, coff, head_dim, capacity, ds->num_sms);
-        floats = pl.partial_floats;
-    }
+    csa::BwdPlan plan;
+    e = csa::plan_bwd(ratio, coff, head_dim, capacity, ds->num_sms, &plan);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "backward plan");
     void *partial = nullptr;
-    e = cudaMallocFromPoolAsync(&partial, (size_t)floats * sizeof(float), ds->pool, st);
+    e = cudaMallocFromPoolAsync(&partial, (size_t)plan.floats * sizeof(float), ds->pool, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward workspace");
-    if (r128)
-        e = csa::launch_bwd_r128(p, static_cast<float *>(partial), r128_blocks, ds->status, st);
-    else if (generic)
-        e = csa::launch_bwd_generic(p, gp, static_cast<float *>(partial), ds->status, st);
-    else if (streamed)
-        e = csa::launch_bwd_stream(p, sp, static_cast<float *>(partial), ds->status, st);
-    else
-        e = csa::launch_bwd_small(p, pl, static_cast<float *>(partial), st);
+    e = csa::launch_bwd(p, plan, static_cast<float *>(partial), ds->status, st);
     cudaError_t e2 = cudaFreeAsync(partial, st);
     if (e != cudaSuccess)
         return cuda_fail(e, "backward launch");
@@ -502,11 +550,11 @@ int csa_selftest_bounded_wait(int64_t limit_ns, void *stream)
 {
     if (limit_ns < 0 || limit_ns > 1000000000ll)
         return fail(CSA_ERR_INVALID_VALUE, "limit_ns must be in [0, 1e9] (got %lld)", (long long)limit_ns);
-    DeviceState *ds = nullptr;
-    cudaError_t e = device_state(&ds);
+    unsigned *word = nullptr;
+    cudaError_t e = csa::status_word(&word);
     if (e != cudaSuccess)
-        return cuda_fail(e, "device set-up");
-    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(ds->status, (uint64_t)limit_ns);
+        return cuda_fail(e, "status word");
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(word, (uint64_t)limit_ns);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return cuda_fail(e, "self-test launch");
@@ -515,18 +563,79 @@ int csa_selftest_bounded_wait(int64_t limit_ns, void *stream)
 
 int csa_device_status(int clear)
 {
-    DeviceState *ds = nullptr;
-    cudaError_t e = device_state(&ds);
+    unsigned *status = nullptr;
+    cudaError_t e = csa::status_word(&status);
     if (e != cudaSuccess)
-        return cuda_fail(e, "device set-up");
+        return cuda_fail(e, "status word");
     unsigned word = 0;
-    e = cudaMemcpy(&word, ds->status, sizeof(word), cudaMemcpyDeviceToHost);
+    e = cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && clear)
-        e = cudaMemset(ds->status, 0, sizeof(word));
+        e = cudaMemset(status, 0, sizeof(word));
     if (e != cudaSuccess)
         return cuda_fail(e, "status read");
     if (word != 0)
         return fail(CSA_ERR_DEVICE_TIMEOUT, "a kernel recorded device status %u (bounded wait expired)", word);
+    return CSA_OK;
+}
+
+int csa_grad_ape_order(int32_t ratio, int32_t coff, int32_t head_dim, int32_t capacity, csa_grad_ape_grouping *out)
+{
+    CSA_TRY(check_common(0, ratio, coff, head_dim, capacity));
+    if (!out)
+        return fail(CSA_ERR_INVALID_VALUE, "out is NULL");
+    int dev = 0, num_sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "device query");
+    csa::BwdPlan b;
+    e = csa::plan_bwd(ratio, coff, head_dim, capacity, num_sms, &b);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "backward plan");
+    csa_grad_ape_grouping o;
+    memset(&o, 0, sizeof(o));
+    o.kind = CSA_GRAD_APE_ROW_BLOCKS;
+    o.final_ranges = 32;
+    switch (b.family) {
+    case csa::kBwdR128:
+        o.kind = CSA_GRAD_APE_CHUNKED;
+        o.blocks = b.r128_blocks;
+        o.partials = b.r128_partials;
+        o.cluster = b.r128_partials > 0 ? b.r128_blocks / b.r128_partials : 1;
+        break;
+    case csa::kBwdGeneric:
+        if (b.gp.staged_blocks > 0) {
+            o.strided = 1;
+            o.blocks = b.gp.staged_blocks;
+            o.lanes = b.gp.staged_lanes;
+        } else {
+            o.blocks = b.gp.groups;
+            o.rows_per_block = b.gp.rows_per_group;
+            o.lanes = b.gp.lanes;
+        }
+        o.cluster = 1;
+        o.flat = 1;
+        o.partials = o.blocks;
+        break;
+    case csa::kBwdStream:
+        o.strided = 1;
+        o.blocks = b.stream_blocks;
+        o.lanes = b.sp.row_lanes;
+        o.cluster = b.sp.cluster;
+        o.flat = 1;
+        o.partials = b.stream_blocks / b.sp.cluster;
+        break;
+    default:
+        o.blocks = b.pl.blocks;
+        o.rows_per_block = b.pl.rows_per_block;
+        o.lanes = b.pl.lanes;
+        o.cluster = b.pl.cluster;
+        o.flat = 0;
+        o.partials = b.pl.partials;
+        break;
+    }
+    *out = o;
     return CSA_OK;
 }
 

@@ -809,8 +809,11 @@ cudaError_t plan_generic(int ratio, int coff, int head_dim, int capacity, int nu
     pl.partial_floats = (int64_t)pl.groups * ratio * coff * head_dim;
     pl.num_sms = num_sms;
     pl.staged_blocks = 0;
+    pl.staged_lanes = 0;
     if (gs_supported(ratio, coff, head_dim)) {  // one partial per row block of the staged kernel
-        cudaError_t e = gs_blocks(true, gs_plan(true, ratio, coff, head_dim), capacity, &pl.staged_blocks);
+        const GsPlan g = gs_plan(true, ratio, coff, head_dim);
+        pl.staged_lanes = g.lanes;
+        cudaError_t e = gs_blocks(true, g, capacity, &pl.staged_blocks);
         if (e != cudaSuccess)
             return e;
         pl.partial_floats = (int64_t)pl.staged_blocks * ratio * coff * head_dim;

@@ -111,6 +111,7 @@ struct GenericPlan {
     int64_t partial_floats; // workspace floats
     int num_sms;
     int staged_blocks;      // > 0: the shared-memory staged kernels, this many row blocks (= partials)
+    int staged_lanes;       // staged kernels: consumer warps per block (row lanes)
 };
 bool generic_supported(int ratio, int coff, int head_dim);
 cudaError_t plan_generic(int ratio, int coff, int head_dim, int capacity, int num_sms, GenericPlan *pl);
@@ -131,6 +132,29 @@ cudaError_t resident_blocks(const void *fn, int threads, size_t smem, int cluste
 // Tiled TMA map of a [rows, C] bf16 row-major tensor at ptr with [box_rows x
 // box_cols] boxes (no swizzle, 256-byte L2 promotion).
 cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int box_cols, int box_rows);
+
+// The backward's kernel family and plan for one shape on the current device: one
+// computation shared by csa_compress_bwd, csa_compress_bwd_noalloc and
+// csa_grad_ape_order, so that the reported grad_ape grouping is the launched one.
+enum BwdFamily { kBwdR128 = 0, kBwdGeneric = 1, kBwdStream = 2, kBwdSmall = 3 };
+struct BwdPlan {
+    BwdFamily family;
+    StreamPlan sp;
+    SmallBwdPlan pl;
+    GenericPlan gp;
+    int r128_blocks;     // ratio 128: grid width
+    int r128_partials;   // ratio 128: grad_ape partials
+    int stream_blocks;   // streamed: exact grid width (row blocks per column tile)
+    int64_t floats;      // grad_ape partial floats the launch needs (an upper bound)
+};
+cudaError_t plan_bwd(int ratio, int coff, int head_dim, int capacity, int num_sms, BwdPlan *out);
+cudaError_t launch_bwd(const BwdParams &p, const BwdPlan &plan, float *partial, unsigned *status,
+                       cudaStream_t st);
+
+// Per-device status word of the bounded waits: a word of the library's own device
+// memory (zero when the device code is loaded), looked up once per device.  No
+// allocation.
+cudaError_t status_word(unsigned **word);
 
 // Records a status and the thread-local message returned by csa_last_error_message().
 int fail_status(int status, const char *fmt, ...);

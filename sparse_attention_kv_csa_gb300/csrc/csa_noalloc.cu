@@ -31,22 +31,22 @@
 // head_dim 512 instead of 19).
 static constexpr size_t kScratchFloats = 1536u * 1024u;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
-// Status word of the bounded waits of calls made through this entry point.
-static __device__ __align__(256) unsigned g_noalloc_status[64];
 
 namespace {
 
+// Per-device set-up: the array's device address and the SM count.  Marked done
+// only when it succeeds, so that a failed first call (say, one made during stream
+// capture) is retried by the next call instead of disabling the entry point.
 struct NoAllocDevice {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
+    bool ready = false;
     float *scratch = nullptr;
-    unsigned *status = nullptr;
     int num_sms = 0;
 };
 constexpr int kMaxDevices = 64;
 NoAllocDevice g_na[kMaxDevices];
+std::mutex g_na_mu;
 
-cudaError_t noalloc_device(NoAllocDevice **out)
+cudaError_t noalloc_device(NoAllocDevice *out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -54,19 +54,24 @@ cudaError_t noalloc_device(NoAllocDevice **out)
         return e;
     if (dev < 0 || dev >= kMaxDevices)
         return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> g(g_na_mu);
     NoAllocDevice &d = g_na[dev];
-    std::call_once(d.once, [&d, dev]() {
+    if (!d.ready) {
         // The array's name is a host-side stand-in: ask the runtime for its device
         // address on this (current) device.
-        cudaError_t err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.scratch), g_noalloc_scratch);
-        if (err == cudaSuccess)
-            err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_noalloc_status);
-        if (err == cudaSuccess)
-            err = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
-        d.err = err;
-    });
-    *out = &d;
-    return d.err;
+        float *scratch = nullptr;
+        int num_sms = 0;
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&scratch), g_noalloc_scratch);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        d.scratch = scratch;
+        d.num_sms = num_sms;
+        d.ready = true;
+    }
+    *out = d;
+    return cudaSuccess;
 }
 
 int check_ptr(const void *p, const char *name, uintptr_t align)
@@ -110,66 +115,41 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
     if ((rc = check_ptr(dape, "dape", 16)) != CSA_OK)
         return rc;
 
-    NoAllocDevice *nd = nullptr;
+    NoAllocDevice nd;
     cudaError_t e = noalloc_device(&nd);
+    unsigned *status = nullptr;
+    if (e == cudaSuccess)  // the same word csa_device_status() reads
+        e = csa::status_word(&status);
     if (e != cudaSuccess)
         return csa::fail_status(CSA_ERR_CUDA, "no-alloc set-up: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
 
     csa::BwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim,
                      capacity, n_tokens, grad_out, dkv, dscore, dape};
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const bool r128 = csa::r128_supported(ratio, coff, head_dim);
-    const bool generic = !r128 && ratio != 4;
-    const bool streamed = !r128 && !generic && csa::stream_supported(ratio, coff, head_dim);
-    csa::StreamPlan sp{};
-    csa::SmallBwdPlan pl{};
-    csa::GenericPlan gp{};
-    int64_t floats = 0;
-    int r128_blocks = 0;
-    if (r128) {
-        int partials = 0;
-        e = csa::r128_bwd_partials(coff, head_dim, capacity, &partials, &r128_blocks);
-        if (e != cudaSuccess)
-            return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
-        floats = (int64_t)partials * ratio * coff * head_dim;
+    csa::BwdPlan plan;
+    e = csa::plan_bwd(ratio, coff, head_dim, capacity, nd.num_sms, &plan);
+    if (e != cudaSuccess)
+        return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
+    int64_t floats = plan.floats;
+    const int64_t per = (int64_t)ratio * coff * head_dim;
+    if (plan.family == csa::kBwdR128 && floats > (int64_t)kScratchFloats && per <= (int64_t)kScratchFloats &&
+        plan.r128_partials > 0) {
         // More partials than the array holds: fewer row blocks per column tile
         // (each walks more rows; one partial per cluster of blocks).
-        const int64_t per = (int64_t)ratio * coff * head_dim;
-        if (floats > (int64_t)kScratchFloats && per <= (int64_t)kScratchFloats && partials > 0) {
-            const int cluster = r128_blocks / partials;
-            const int fit = (int)((int64_t)kScratchFloats / per);
-            r128_blocks = fit * cluster;
-            floats = (int64_t)fit * per;
-        }
-    } else if (generic) {
-        e = csa::plan_generic(ratio, coff, head_dim, capacity, nd->num_sms, &gp);
-        if (e != cudaSuccess)
-            return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
-        floats = gp.partial_floats;
-    } else if (streamed) {
-        sp = csa::plan_stream(true, ratio, coff, head_dim, capacity, nd->num_sms);
-        int blocks = 0;
-        e = csa::stream_bwd_blocks(ratio, coff, sp, capacity, &blocks);
-        if (e != cudaSuccess)
-            return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
-        floats = (int64_t)(blocks / sp.cluster) * ratio * coff * head_dim;
-    } else {
-        pl = csa::plan_bwd_small(ratio, coff, head_dim, capacity, nd->num_sms);
-        floats = pl.partial_floats;
+        const int cluster = plan.r128_blocks / plan.r128_partials;
+        const int fit = (int)((int64_t)kScratchFloats / per);
+        plan.r128_blocks = fit * cluster;
+        plan.r128_partials = fit;
+        floats = (int64_t)fit * per;
+    } else if (plan.family == csa::kBwdStream) {
+        // the exact grid's partials (the regular call sizes its pool block by an upper bound)
+        floats = (int64_t)(plan.stream_blocks / plan.sp.cluster) * per;
     }
     if (floats > (int64_t)kScratchFloats)
         return csa::fail_status(CSA_ERR_TOO_LARGE,
                                 "csa_compress_bwd_noalloc needs %lld floats of grad_ape scratch for this shape; "
                                 "its fixed array holds %lld (use csa_compress_bwd)",
                                 (long long)floats, (long long)kScratchFloats);
-    if (r128)
-        e = csa::launch_bwd_r128(p, nd->scratch, r128_blocks, nd->status, st);
-    else if (generic)
-        e = csa::launch_bwd_generic(p, gp, nd->scratch, nd->status, st);
-    else if (streamed)
-        e = csa::launch_bwd_stream(p, sp, nd->scratch, nd->status, st);
-    else
-        e = csa::launch_bwd_small(p, pl, nd->scratch, st);
+    e = csa::launch_bwd(p, plan, nd.scratch, status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return csa::fail_status(CSA_ERR_CUDA, "backward launch: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
     return CSA_OK;

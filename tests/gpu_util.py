@@ -73,3 +73,30 @@ def tolerance_report(got_bits, ref64):
     ref_bits = w.to_bf16_bits(ref64)
     diff = got_bits != ref_bits
     return int(diff.sum()), float(np.abs(F(got_bits).astype(np.float64) - F(ref_bits)).max()) if diff.size else 0.0
+
+
+def same_f32_nan_aware(a, b):
+    """fp32 bit patterns equal, except that any two NaNs count as equal."""
+    a, b = np.asarray(a, np.float32), np.asarray(b, np.float32)
+    na, nb = np.isnan(a), np.isnan(b)
+    return np.array_equal(na, nb) and np.array_equal(a[~na].view(np.uint32), b[~nb].view(np.uint32))
+
+
+def check_dape(c, dape, csa, grouping=None):
+    """grad_ape against the oracle.  Every ratio but 128: bit for bit equal to the
+    oracle's fp32 sum taken in the grouping the library reports for this shape
+    (csa_grad_ape_order; the rows, leaves and combination are formed by the oracle
+    from the rules stated in include/csa.h).  Ratio 128 (chunked sums, tolerance
+    contract): within 1e-5 (normwise) of the fp64 oracle.  Returns the grouping."""
+    import oracle
+    g = grouping or csa.csa_grad_ape_order(c.ratio, c.coff, c.head_dim, c.capacity)
+    if g["kind"] == "row_blocks":
+        want = oracle.case_dape_grouped_f32(c, g)
+        assert same_f32_nan_aware(dape, want), (
+            "grad_ape differs from the grouped fp32 oracle in %d of %d entries (max |diff| %.3g)"
+            % (int((dape.view(np.uint32) != want.view(np.uint32)).sum()), dape.size,
+               float(np.nanmax(np.abs(dape.astype(np.float64) - want)))))
+    else:
+        _, _, d64 = oracle.case_bwd_f64(c)
+        assert np.abs(dape - d64).max() <= 1e-5 * max(np.abs(d64).max(), 1e-30)
+    return g

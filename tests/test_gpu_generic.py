@@ -1,6 +1,8 @@
 """The generic-ratio kernels (every ratio in [1, 128] other than 4 and 128): the
 library's sequential fp32 order, so out / grad_kv / grad_score are bitwise equal to
-the fp32 oracle; grad_ape within 1e-5 (normwise) of the fp64 oracle.  Ragged packs
+the fp32 oracle; grad_ape bitwise equal to the oracle's fp32 sum in the grouping
+the library reports (csa_grad_ape_order) and within 1e-5 (normwise) of the fp64
+oracle.  Ragged packs
 per ratio: tails, empty segments, segments shorter than the ratio, exact
 multiples, leading tokens, token padding, padding rows."""
 import numpy as np
@@ -8,7 +10,7 @@ import pytest
 
 import csa_workloads as w
 import oracle
-from gpu_util import Dev, run_bwd, run_fwd
+from gpu_util import Dev, check_dape, run_bwd, run_fwd
 
 pytestmark = pytest.mark.gpu
 
@@ -33,6 +35,7 @@ def check(c, csa):
     dkv, dsc, dape = run_bwd(d, csa)
     want = oracle.case_bwd_f32(c)
     assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+    check_dape(c, dape, csa)
     _, _, d64 = oracle.case_bwd_f64(c)
     assert np.all(np.abs(dape - d64) <= 1e-5 * max(np.abs(d64).max(), 1e-30))
 

@@ -4,8 +4,9 @@ Contract ("CSA Fused Compressor" page, Numerics; ratio-4 family): out, grad_kv
 and grad_score equal, bit for bit, the oracle's fp32 result computed in the
 kernels' operation order; against the fp64 oracle they differ on at most
 max(1, 0.1%) of elements with max_abs <= 1.6e-2 (x 2^k, x 2^2k under 2^k input
-scaling); grad_ape is within 1e-5 (normwise) of the fp64 oracle and within the
-summation-order bound of the fp32 one.  Every output is NaN-canary prefilled, so
+scaling); grad_ape equals, bit for bit, the oracle's fp32 sum taken in the
+grouping the library reports (csa_grad_ape_order), and is within 1e-5 (normwise)
+of the fp64 oracle and within the summation-order bound of the plain fp32 sum.  Every output is NaN-canary prefilled, so
 a slot the kernels fail to write shows up as a mismatch.
 """
 import numpy as np
@@ -13,7 +14,7 @@ import pytest
 
 import csa_workloads as w
 import oracle
-from gpu_util import Dev, F, run_bwd, run_fwd, same_bits_nan_aware, tolerance_report
+from gpu_util import Dev, F, check_dape, run_bwd, run_fwd, same_bits_nan_aware, tolerance_report
 
 pytestmark = pytest.mark.gpu
 
@@ -47,6 +48,7 @@ def check_against_oracle(c, csa, scale=1.0, overflow=False):
     assert same_bits_nan_aware(out, ref["out"]), "forward differs from the fp32 oracle"
     assert same_bits_nan_aware(dkv, ref["bwd"][0]), "grad_kv differs from the fp32 oracle"
     assert same_bits_nan_aware(dsc, ref["bwd"][1]), "grad_score differs from the fp32 oracle"
+    check_dape(c, dape, csa)
     if overflow:
         assert np.isnan(F(out)).any()
         assert np.array_equal(np.isnan(dape), np.isnan(ref["bwd"][2]))
@@ -71,6 +73,8 @@ def test_tiny_bitwise(csa):
     assert np.array_equal(out, oracle.case_fwd_f32(c))
     want = oracle.case_bwd_f32(c)
     assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+    g = check_dape(c, dape, csa)
+    assert g["kind"] == "row_blocks"
     _, _, d64 = oracle.case_bwd_f64(c)
     assert np.abs(dape - d64).max() <= 1e-5 * np.abs(d64).max()
 
@@ -165,6 +169,7 @@ def test_small_layouts_bitwise(csa, coff, head_dim, li):
     dkv, dsc, dape = run_bwd(d, csa)
     want = oracle.case_bwd_f32(c)
     assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+    check_dape(c, dape, csa)
     _, _, d64 = oracle.case_bwd_f64(c)
     assert np.all(np.abs(dape - d64) <= 1e-5 * max(np.abs(d64).max(), 1e-30))
 
@@ -186,6 +191,7 @@ def test_stream_row_lanes_bitwise(csa, coff, head_dim, li):
     dkv, dsc, dape = run_bwd(d, csa)
     want = oracle.case_bwd_f32(c)
     assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+    check_dape(c, dape, csa)
     _, _, d64 = oracle.case_bwd_f64(c)
     assert np.all(np.abs(dape - d64) <= 1e-5 * max(np.abs(d64).max(), 1e-30))
 
@@ -198,6 +204,7 @@ def test_wide_heads_bitwise(csa, head_dim):
     dkv, dsc, dape = run_bwd(d, csa)
     want = oracle.case_bwd_f32(c)
     assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+    check_dape(c, dape, csa)
 
 
 def test_capacity_zero(csa):

@@ -13,6 +13,7 @@ import pytest
 import oracle
 import test_oracle_bruteforce as B
 import test_oracle_exp as E
+import test_oracle_grouped as G
 import test_oracle_pins as P
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "csa_oracle.c")
@@ -26,6 +27,10 @@ MUTATIONS = {
     "denominator_drops_terms": ("        den = den + ek;", "        den = ek;"),
     "grad_score_sign_flipped": ("                float ds = p * (g * v - go);",
                                 "                float ds = p * (go - g * v);"),
+    "grouped_grad_ape_sign_flipped": ("                float ds_k = p * (g * v - go);",
+                                      "                float ds_k = p * (go - g * v);"),
+    "grouped_grad_ape_skips_first_blocks": ("        const int32_t leaf = leaf_of_row[r];",
+                                            "        const int32_t leaf = leaf_of_row[r];\n        if (ri.first)\n            continue;"),
     "fp64_grad_score_sign_flipped": ("                double ds = p[k] * g * (v - o);",
                                      "                double ds = p[k] * g * (o - v);"),
     "padding_rows_carry_gradient": ("            continue; /* padding rows: incoming gradient ignored */",
@@ -57,6 +62,8 @@ def pins():
         ("fd1", lambda: P.test_backward_matches_central_finite_differences(1)),
         ("fd2", lambda: P.test_backward_matches_central_finite_differences(2)),
         ("bruteforce_r3c2", lambda: B.test_window_map_bruteforce(3, 2)),
+        ("grouped_rows", lambda: G.test_one_row_leaves_are_the_rows_ds(*G.CASES[0])),
+        ("grouped_single", G.test_single_leaf_is_the_plain_sum),
     ]
     return out
 
