@@ -244,6 +244,13 @@ SPECS = {
     # 8 segments of 4096 tokens (2048 rows), 64 padding rows
     "r16c2d512_8x4096": lambda seed=0: dict(name="r16c2d512_8x4096", ratio=16, coff=2, head_dim=512,
                                             seqlens=[4096] * 8, extra_rows=64),
+    # windows of more than 64 positions at ratios other than 128 (chunked kernels):
+    # ratio 64 with the overlapping window (128 positions), 8 x 4096 tokens, 16
+    # padding rows; ratio 96 with the own-block window, 8 x 6144 tokens
+    "r64c2d512_8x4096": lambda seed=0: dict(name="r64c2d512_8x4096", ratio=64, coff=2, head_dim=512,
+                                            seqlens=[4096] * 8, extra_rows=16),
+    "r96c1d512_8x6144": lambda seed=0: dict(name="r96c1d512_8x6144", ratio=96, coff=1, head_dim=512,
+                                            seqlens=[6144] * 8),
 }
 
 

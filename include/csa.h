@@ -56,10 +56,12 @@
  *
  * Supported set (csa_check_support): coff in {1, 2}; ratio == 128 with head_dim a
  * multiple of 64 in [64, 8192]; every other ratio in [1, 128] with head_dim a
- * multiple of 8 in [8, 8192].  Numerics per ratio family (section Numerics): ratio
- * 128 sums the window in fixed chunks with the hardware exp2 (deterministic, equal
- * to the sequential evaluation within final-bf16 rounding tolerance); every other
- * ratio (4 on its own kernels, the rest on the generic ones) computes each window
+ * multiple of 8 in [8, 8192].  Numerics per window (section Numerics): a window of
+ * more than 64 positions with head_dim a multiple of 64 -- ratio 128, and ratios
+ * 33-127 with coff 2 or 65-127 with coff 1 -- is summed in fixed chunks with the
+ * hardware exp2, the page's ratio-128 evaluation (deterministic, equal to the
+ * sequential evaluation within final-bf16 rounding tolerance); every other shape
+ * (ratio 4 on its own kernels, the rest on the generic ones) computes each window
  * in ascending position order with the library's exp, bitwise equal to a plain
  * sequential fp32 evaluation.
  */
@@ -141,12 +143,13 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * could block, a plug-in that may not use the CUDA allocator.
  *
  * Same arguments, results and errors as csa_compress_bwd (bitwise the same
- * outputs, but see below for ratio 128's grad_ape), except that the grad_ape partial sums go to a fixed 6 MiB array in
+ * outputs, but see below for the chunked windows' grad_ape), except that the grad_ape partial sums go to a fixed 6 MiB array in
  * the library's device code instead of the library's memory pool.  That array
  * occupies 6 MiB on every GPU that loads the library, until the process exits.
  * Where the regular backward's grid would need more partial storage than the
- * array holds, ratio 128 runs with fewer row blocks (same grad_kv / grad_score
- * bits; grad_ape summed in another fixed grouping); a shape whose single partial
+ * array holds, the chunked windows (ratio 128, and other ratios with more than 64
+ * window positions) run with fewer row blocks (same grad_kv / grad_score bits;
+ * grad_ape summed in another fixed grouping); a shape whose single partial
  * does not fit is rejected with CSA_ERR_TOO_LARGE before anything is launched (on
  * a 152-SM GB300 every shape fits except ratio 128 with coff 2 and head_dim above
  * 6144, and other ratios with ratio * coff * head_dim above 1572864).  No
@@ -161,7 +164,7 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * set-up again.  Bounded device waits that expire in this call's kernels are
  * recorded in the same per-device status word as those of every other call, so
  * csa_device_status() reports them (CSA_ERR_DEVICE_TIMEOUT).  The grad_ape
- * grouping is csa_grad_ape_order's for every ratio but 128.
+ * grouping is csa_grad_ape_order's for every shape outside the chunked windows.
  */
 CSA_API int csa_compress_bwd_noalloc(const void *kv, const void *score, const float *ape,
                              const int32_t *cu_seqlens, const int32_t *cu_seqlens_comp, int32_t n_seg,
@@ -210,9 +213,11 @@ CSA_API const char *csa_last_error_message(void);
  *      from +0 in ascending order; then the 32 range sums are added in pairs
  *      (t, t^1), then (t, t^2), (t, t^4), (t, t^8), (t, t^16): a balanced binary
  *      tree over the ranges in order.
- * kind == CSA_GRAD_APE_CHUNKED (ratio 128): every sum of the ratio-128 kernels is
- * taken in fixed chunks (section ratio=128 of the page); grad_ape is deterministic
- * but has no bitwise contract.  blocks, partials and cluster describe the grid.
+ * kind == CSA_GRAD_APE_CHUNKED (the chunked windows above: ratio 128, and other
+ * ratios with more than 64 window positions and head_dim a multiple of 64): every
+ * sum of those kernels is taken in fixed chunks (section ratio=128 of the page);
+ * grad_ape is deterministic but has no bitwise contract.  blocks, partials and
+ * cluster describe the grid.
  *
  * Errors: those of csa_check_support for the shape, CSA_ERR_INVALID_VALUE for a
  * NULL out, CSA_ERR_CUDA if the device cannot be queried.

@@ -352,10 +352,10 @@ cudaError_t plan_bwd(int ratio, int coff, int head_dim, int capacity, int num_sm
 {
     BwdPlan b{};
     cudaError_t e = cudaSuccess;
-    if (r128_supported(ratio, coff, head_dim)) {
-        b.family = kBwdR128;
-        e = r128_bwd_partials(coff, head_dim, capacity, &b.r128_partials, &b.r128_blocks);
-        b.floats = (int64_t)b.r128_partials * ratio * coff * head_dim;
+    if (chunked_supported(ratio, coff, head_dim)) {
+        b.family = kBwdChunked;
+        e = chunked_bwd_partials(ratio, coff, head_dim, capacity, &b.ch_partials, &b.ch_blocks);
+        b.floats = (int64_t)b.ch_partials * ratio * coff * head_dim;
     } else if (ratio != 4) {
         b.family = kBwdGeneric;
         e = plan_generic(ratio, coff, head_dim, capacity, num_sms, &b.gp);
@@ -377,7 +377,7 @@ cudaError_t plan_bwd(int ratio, int coff, int head_dim, int capacity, int num_sm
 cudaError_t launch_bwd(const BwdParams &p, const BwdPlan &b, float *partial, unsigned *status, cudaStream_t st)
 {
     switch (b.family) {
-    case kBwdR128: return launch_bwd_r128(p, partial, b.r128_blocks, status, st);
+    case kBwdChunked: return launch_bwd_chunked(p, partial, b.ch_blocks, status, st);
     case kBwdGeneric: return launch_bwd_generic(p, b.gp, partial, status, st);
     case kBwdStream: return launch_bwd_stream(p, b.sp, partial, status, st);
     default: return launch_bwd_small(p, b.pl, partial, st);
@@ -442,8 +442,8 @@ int csa_compress_fwd(const void *kv, const void *score, const float *ape, const 
         return cuda_fail(e, "device set-up");
     csa::FwdParams p{kv, score, ape, cu_seqlens, cu_seqlens_comp, n_seg, ratio, coff, head_dim, capacity, out};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (csa::r128_supported(ratio, coff, head_dim))
-        e = csa::launch_fwd_r128(p, ds->status, st);
+    if (csa::chunked_supported(ratio, coff, head_dim))
+        e = csa::launch_fwd_chunked(p, ds->status, st);
     else if (ratio != 4)
         e = csa::launch_fwd_generic(p, ds->status, ds->num_sms, st);
     else if (csa::stream_supported(ratio, coff, head_dim))
@@ -598,11 +598,11 @@ int csa_grad_ape_order(int32_t ratio, int32_t coff, int32_t head_dim, int32_t ca
     o.kind = CSA_GRAD_APE_ROW_BLOCKS;
     o.final_ranges = 32;
     switch (b.family) {
-    case csa::kBwdR128:
+    case csa::kBwdChunked:
         o.kind = CSA_GRAD_APE_CHUNKED;
-        o.blocks = b.r128_blocks;
-        o.partials = b.r128_partials;
-        o.cluster = b.r128_partials > 0 ? b.r128_blocks / b.r128_partials : 1;
+        o.blocks = b.ch_blocks;
+        o.partials = b.ch_partials;
+        o.cluster = b.ch_partials > 0 ? b.ch_blocks / b.ch_partials : 1;
         break;
     case csa::kBwdGeneric:
         if (b.gp.staged_blocks > 0) {

@@ -1,29 +1,35 @@
-// Compressor kernels for ratio 128 ("CSA Fused Compressor", cuDNN frontend docs,
-// sections Semantics and "ratio=128"): a window of 128 (coff 1) or 256 (coff 2)
-// tokens per output row -- too long for one thread -- is split into chunks of 8
-// window positions held by different threads and merged in a fixed order.
+// Chunked Compressor kernels for windows of more than 64 positions ("CSA Fused
+// Compressor", cuDNN frontend docs, sections Semantics and "ratio=128"): ratio 128
+// (window 128 with coff 1, 256 with coff 2), and every other ratio whose window
+// exceeds 64 positions (33-127 with coff 2, 65-127 with coff 1), head_dim a
+// multiple of 64.  A window this long is split into chunks of 8 window positions
+// held by different threads and merged in a fixed order.
 //
 // Per thread block: a column tile of TC = 64 / coff columns, persistent over the
 // rows b, b + gridDim.x, ...  One producer warp streams, per row, the window's
-// [128 tokens x TC columns] boxes of kv and score (one box per array and part)
+// [ratio tokens x TC columns] boxes of kv and score (one box per array and part)
 // with 2-D TMA tensor copies into a shared-memory ring tracked by mbarriers (and,
-// in the backward, the grad_out row with a bulk copy).  Eight consumer warps: a
-// thread owns a group g of 4 columns and a chunk c of NC = 16*coff chunks, whose
-// window positions are k = c, c + NC, c + 2*NC, ... (8 of them), so that the
-// lanes of a warp read consecutive box rows (no bank conflicts) and each
-// thread's APE values stay in registers.
+// in the backward, the grad_out row with a bulk copy).  NC chunks (16 for windows
+// of up to 128 positions, 32 up to 256): a thread owns a group g of 4 columns and
+// a chunk c, whose window positions are k = c, c + NC, c + 2*NC, ... (8 of them;
+// those at or past the window's end are skipped), so that the lanes of a warp
+// read consecutive box rows (no bank conflicts) and each thread's APE values stay
+// in registers.  Ratio 128 is compiled with the ratio as a constant; the other
+// ratios take it at run time.
 //
 // Order of the arithmetic (the page's ratio-128 family: a deterministic chunked
-// order, checked against the plain sequential oracle by tolerance):
+// order, checked against the plain sequential oracle by tolerance; the library
+// applies the same contract to every window of more than 64 positions):
 //   s_k = score + ape;  m = max over all valid k (exact: chunk maxima, then over
-//   the warp's chunks by shuffles, then over the eight warps);
+//   the warp's chunks by shuffles, then over the consumer warps);
 //   e_k = 2^(s_k*log2(e) - m*log2(e)) on the multi-function unit (ex2.approx, as
 //   the page's ratio-128 kernels do: ~2^-22 relative error, far below the final
 //   bf16 rounding);
 //   den_c = ((+0 + e_c) + e_c+NC) + ... within chunk c, num_c = fma chain;
 //   chunk sums added over the warp's chunks by a fixed xor-shuffle tree, warp sums
-//   added in ascending warp pairs and then by a fixed xor-shuffle tree over the
-//   threads of a column;  inv = 1/den rounded;  o = num * inv;  out = bf16(o).
+//   added in ascending warp order by the threads of a column and then by a fixed
+//   xor-shuffle tree over those threads;  inv = 1/den rounded;  o = num * inv;
+//   out = bf16(o).
 // Backward per valid k: p = e_k * inv;  grad_kv = bf16(g*p);
 //   ds = p*fma(g, kv, -g*o);  grad_score = bf16(ds); grad_ape as in the other kernels
 //   (per-thread sums over its rows, cluster merge in rank order, fixed-order
@@ -41,42 +47,37 @@
 
 namespace cg = cooperative_groups;
 
-#ifndef CSA_R128_BWD_CLUSTER
-#define CSA_R128_BWD_CLUSTER 1
-#endif
-
 namespace csa {
 
 namespace {
 
-constexpr int kR = 128;  // ratio
-constexpr int kKC = 8;   // window positions per chunk (per thread)
+constexpr int kKC = 8;  // window positions per chunk (per thread)
 
 // Backward layout per window form.  coff 1: APE and the kv words in registers,
 // the stage released as soon as it is read, one block per SM (registers), a
 // four-stage ring.  coff 2 (twice the column tiles per row): "lean" -- APE from a
 // shared tile, kv read again from the stage, which stays held until the row's
 // gradients are written -- so that two blocks fit per SM.  Each measured faster
-// for its form on GB300.
+// for its form on GB300 at ratio 128.
 template <int COFF>
 constexpr bool kBwdLean = COFF == 2;
 
-template <int COFF>
+// Block geometry for a form and a chunk count (the window's bucket).
+template <int COFF, int NCB>
 struct Geo {
     static constexpr int TC = 64 / COFF;      // columns per block tile
     static constexpr int G = TC / 4;          // column groups (4 columns each)
     static constexpr int CPW = 32 / G;        // chunks per warp
-    static constexpr int W = COFF * kR;       // window
-    static constexpr int NC = W / kKC;        // chunks
-    static constexpr int CW = NC / CPW;       // consumer warps (8)
+    static constexpr int NC = NCB;            // chunks
+    static constexpr int WMAX = kKC * NC;     // longest window of the bucket
+    static constexpr int CW = NC / CPW;       // consumer warps
     static constexpr int CT = CW * 32;        // consumer threads
     static constexpr int THREADS = CT + 32;   // + one producer warp
     static constexpr int RS = TC + 4;         // row stride of the merge buffers
-    static constexpr int BOX_BYTES = kR * TC * 2;
-    static constexpr int WIN_BYTES = 2 * COFF * BOX_BYTES;
+    static_assert(CW * CPW == NC, "chunks per warp");
 };
 
-struct R128Args {
+struct ChArgs {
     const uint16_t *kv;
     const uint16_t *score;
     const float *ape;
@@ -85,9 +86,52 @@ struct R128Args {
     int n_seg;
     int head_dim;
     int capacity;
+    int ratio;
+    int box_bytes;  // stride of the [ratio x TC] bf16 boxes in a stage (128-byte multiple)
     int stages;
     int stage_bytes;
     unsigned *status;
+};
+
+// The window of a row: the ratio (a constant RC, or taken at run time when RC is
+// 0) and, for window position k = c + NC*i of chunk c, its part (0: the previous
+// block's tokens on the first-half columns, coff 2 only; else the own block) and
+// its token within the part.
+template <int COFF, int NCB, int RC>
+struct Win {
+    int r;
+    int bb;  // box bytes
+    __device__ __forceinline__ Win(const ChArgs &a) : r(RC > 0 ? RC : a.ratio), bb(a.box_bytes) {}
+    __device__ __forceinline__ int ratio() const { return RC > 0 ? RC : r; }
+    // bytes of one box's data, and the stride between boxes in a stage (rounded up
+    // to 128 bytes: TMA tensor copies write 128-byte aligned shared memory)
+    __device__ __forceinline__ int box_data() const { return ratio() * Geo<COFF, NCB>::TC * 2; }
+    __device__ __forceinline__ int box_bytes() const { return RC > 0 ? (RC * Geo<COFF, NCB>::TC * 2 + 127) / 128 * 128 : bb; }
+    __device__ __forceinline__ int win_bytes() const { return 2 * COFF * box_bytes(); }
+    // false for a position past the end of the window (the bucket may be longer)
+    __device__ __forceinline__ bool pos(int c, int i, int &part, int &tok) const
+    {
+        const int k = c + NCB * i, rr = ratio();
+        if (COFF == 1) {
+            part = 0;
+            tok = k;
+        } else {
+            part = k >= rr ? 1 : 0;
+            tok = k - part * rr;
+        }
+        if (RC > 0 && COFF * RC == kKC * NCB)
+            return true;  // the window fills the bucket
+        return k < COFF * rr;
+    }
+    // a position the row reads: inside the window, and not a first block's
+    // previous-block position (coff 2)
+    __device__ __forceinline__ bool valid(int c, int i, bool first) const
+    {
+        int part, tok;
+        return pos(c, i, part, tok) && !(COFF == 2 && part == 0 && first);
+    }
+    // box of array arr (0 kv, 1 score) and part p in a stage
+    __device__ __forceinline__ int box_offset(int arr, int part) const { return (arr * COFF + part) * box_bytes(); }
 };
 
 struct Meta {
@@ -100,33 +144,32 @@ struct Meta {
     int pad;
 };
 
-template <int COFF>
-struct R128Smem {
+template <int COFF, int NCB>
+struct ChSmem {
     unsigned char *stages;
     float *mx;   // [2][CW][RS]  warp maxima
     float *den;  // [2][CW][RS]  warp sums
     float *num;  // [2][CW][RS]
     float *fin;  // [2][2][TC]  (inv, o) for the backward
-    float *apet; // [W][TC]  the backward's APE tile (null in the forward)
+    float *apet; // [WMAX][TC]  the backward's APE tile (null in the forward)
     Meta *meta;
     uint64_t *full;
     uint64_t *empty;
 };
 
-template <int COFF>
-__host__ __device__ size_t r128_smem_bytes(int stages, int stage_bytes, bool ape_tile)
+template <int COFF, int NCB>
+__host__ __device__ size_t ch_smem_bytes(int stages, int stage_bytes, bool ape_tile)
 {
-    using G = Geo<COFF>;
+    using G = Geo<COFF, NCB>;
     return (size_t)stages * stage_bytes + 3 * 2 * G::CW * G::RS * 4 + 2 * 2 * G::TC * 4 +
-           (ape_tile ? (size_t)G::W * G::TC * 4 : 0) + sizeof(Meta) * stages + 16 * stages + 16;
+           (ape_tile ? (size_t)G::WMAX * G::TC * 4 : 0) + sizeof(Meta) * stages + 16 * stages + 16;
 }
 
-template <int COFF>
-__device__ __forceinline__ R128Smem<COFF> r128_carve(unsigned char *base, int stages, int stage_bytes,
-                                                     bool ape_tile)
+template <int COFF, int NCB>
+__device__ __forceinline__ ChSmem<COFF, NCB> ch_carve(unsigned char *base, int stages, int stage_bytes, bool ape_tile)
 {
-    using G = Geo<COFF>;
-    R128Smem<COFF> s;
+    using G = Geo<COFF, NCB>;
+    ChSmem<COFF, NCB> s;
     s.stages = base;
     unsigned char *p = base + (size_t)stages * stage_bytes;
     s.mx = reinterpret_cast<float *>(p);
@@ -134,43 +177,29 @@ __device__ __forceinline__ R128Smem<COFF> r128_carve(unsigned char *base, int st
     s.num = s.den + 2 * G::CW * G::RS;
     s.fin = s.num + 2 * G::CW * G::RS;
     s.apet = ape_tile ? s.fin + 2 * 2 * G::TC : nullptr;
-    p = reinterpret_cast<unsigned char *>(s.fin + 2 * 2 * G::TC + (ape_tile ? G::W * G::TC : 0));
+    p = reinterpret_cast<unsigned char *>(s.fin + 2 * 2 * G::TC + (ape_tile ? G::WMAX * G::TC : 0));
     s.meta = reinterpret_cast<Meta *>(p);
     s.full = reinterpret_cast<uint64_t *>(s.meta + stages);
     s.empty = s.full + stages;
     return s;
 }
 
-// Box of array arr (0 kv, 1 score) and part p in a stage.
-template <int COFF>
-__device__ __forceinline__ int box_offset(int arr, int part)
-{
-    return (arr * COFF + part) * Geo<COFF>::BOX_BYTES;
-}
-
-// Window position k = c + NC*i of chunk c: its part and its token within the part.
-template <int COFF>
-__device__ __forceinline__ void position(int c, int i, int &part, int &tok)
-{
-    const int k = c + Geo<COFF>::NC * i;
-    part = k / kR;
-    tok = k - part * kR;
-}
-
 // ----------------------------------------------------------------- producer
 
-template <int COFF, bool BWD>
-__device__ void r128_produce(const R128Args &a, const R128Smem<COFF> &s, const CUtensorMap *tm_kv,
-                             const CUtensorMap *tm_sc, int c0, int row0, int rstride, int rend,
-                             const uint16_t *__restrict__ grad_out)
+template <int COFF, int NCB, int RC, bool BWD>
+__device__ void ch_produce(const ChArgs &a, const ChSmem<COFF, NCB> &s, const CUtensorMap *tm_kv,
+                           const CUtensorMap *tm_sc, int c0, int row0, int rstride, int rend,
+                           const uint16_t *__restrict__ grad_out)
 {
-    using G = Geo<COFF>;
+    using G = Geo<COFF, NCB>;
+    const Win<COFF, NCB, RC> w(a);
+    const int R = w.ratio();
     int issued = 0, st = 0;
     uint32_t ph = 0;
     for (int row = row0; row < rend; row += rstride) {
         if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
             break;
-        const RowMap rm = map_row(row, a.cu, a.cc, a.n_seg, kR);
+        const RowMap rm = map_row(row, a.cu, a.cc, a.n_seg, R);
         Meta &m = s.meta[st];
         m.base = rm.base;
         m.seg = rm.seg;
@@ -181,19 +210,19 @@ __device__ void r128_produce(const R128Args &a, const R128Smem<COFF> &s, const C
         const bool load = BWD ? rm.real : true;
         const int p0 = (COFF == 2 && rm.first) ? 1 : 0;
         const uint32_t bytes =
-            load ? (uint32_t)((COFF - p0) * 2 * G::BOX_BYTES) + (BWD ? (uint32_t)G::TC * 2u : 0u) : 0u;
+            load ? (uint32_t)((COFF - p0) * 2 * w.box_data()) + (BWD ? (uint32_t)G::TC * 2u : 0u) : 0u;
         const uint32_t fb = smem_addr(&s.full[st]);
         mbar_arrive_expect_tx(fb, bytes);
         if (load) {
             const uint32_t dst = smem_addr(s.stages + (size_t)st * a.stage_bytes);
             for (int p = p0; p < COFF; ++p) {
-                const int y = (int)(rm.base + (int64_t)(p - (COFF - 1)) * kR);
+                const int y = (int)(rm.base + (int64_t)(p - (COFF - 1)) * R);
                 const int x = p * a.head_dim + c0;
-                tma_load_2d(dst + box_offset<COFF>(0, p), tm_kv, x, y, fb);
-                tma_load_2d(dst + box_offset<COFF>(1, p), tm_sc, x, y, fb);
+                tma_load_2d(dst + w.box_offset(0, p), tm_kv, x, y, fb);
+                tma_load_2d(dst + w.box_offset(1, p), tm_sc, x, y, fb);
             }
             if (BWD)
-                bulk_g2s(dst + G::WIN_BYTES, grad_out + (int64_t)row * a.head_dim + c0, G::TC * 2, fb);
+                bulk_g2s(dst + w.win_bytes(), grad_out + (int64_t)row * a.head_dim + c0, G::TC * 2, fb);
         }
         ++issued;
         if (++st == a.stages) {
@@ -213,22 +242,20 @@ struct ChunkState {
     float2 e[kKC][2];  // s_k, then e_k
 };
 
-template <int COFF>
-__device__ __forceinline__ bool pos_valid(int c, int i, bool first)
-{
-    int part, tok;
-    position<COFF>(c, i, part, tok);
-    return !(COFF == 2 && part == 0 && first);
-}
-
-template <int COFF>
-__device__ __forceinline__ void r128_load_ape(const R128Args &a, int c, int col, float2 (&ap)[kKC][2])
+// The thread's APE values, [position i][column pair] (positions past the window
+// are not read).
+template <int COFF, int NCB, int RC>
+__device__ __forceinline__ void ch_load_ape(const ChArgs &a, const Win<COFF, NCB, RC> &w, int c, int col,
+                                            float2 (&ap)[kKC][2])
 {
     const int64_t C = (int64_t)COFF * a.head_dim;
 #pragma unroll
     for (int i = 0; i < kKC; ++i) {
         int part, tok;
-        position<COFF>(c, i, part, tok);
+        if (!w.pos(c, i, part, tok)) {
+            ap[i][0] = ap[i][1] = make_float2(0.0f, 0.0f);
+            continue;
+        }
         const float4 v =
             __ldg(reinterpret_cast<const float4 *>(a.ape + tok * C + (int64_t)part * a.head_dim + col));
         ap[i][0] = make_float2(v.x, v.y);
@@ -237,19 +264,18 @@ __device__ __forceinline__ void r128_load_ape(const R128Args &a, int c, int col,
 }
 
 // Reads the thread's positions of one row from the stage and forms s = score + ape.
-template <int COFF>
-__device__ __forceinline__ void r128_load(const unsigned char *stage, int c, int g, bool first,
-                                          const float2 (&ap)[kKC][2], ChunkState &cs)
+template <int COFF, int NCB, int RC>
+__device__ __forceinline__ void ch_load(const Win<COFF, NCB, RC> &w, const unsigned char *stage, int c, int g,
+                                        bool first, const float2 (&ap)[kKC][2], ChunkState &cs)
 {
 #pragma unroll
     for (int i = 0; i < kKC; ++i) {
-        if (!pos_valid<COFF>(c, i, first))
-            continue;
         int part, tok;
-        position<COFF>(c, i, part, tok);
-        const int off = tok * Geo<COFF>::TC * 2 + 8 * g;
-        cs.kv[i] = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(0, part) + off);
-        const uint2 sw = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(1, part) + off);
+        if (!w.pos(c, i, part, tok) || (COFF == 2 && part == 0 && first))
+            continue;
+        const int off = tok * Geo<COFF, NCB>::TC * 2 + 8 * g;
+        cs.kv[i] = *reinterpret_cast<const uint2 *>(stage + w.box_offset(0, part) + off);
+        const uint2 sw = *reinterpret_cast<const uint2 *>(stage + w.box_offset(1, part) + off);
         cs.e[i][0] = add2_bf16x2(sw.x, ap[i][0]);
         cs.e[i][1] = add2_bf16x2(sw.y, ap[i][1]);
     }
@@ -267,22 +293,20 @@ __device__ __forceinline__ float ex2_fast(float x)
 
 // Backward: s = score + ape for the thread's positions, APE from the block's tile
 // (kv is read from the stage again where it is needed).
-template <int COFF>
-__device__ __forceinline__ void r128_load_s(const unsigned char *stage, const float *apet, int c, int g,
-                                            bool first, ChunkState &cs)
+template <int COFF, int NCB, int RC>
+__device__ __forceinline__ void ch_load_s(const Win<COFF, NCB, RC> &w, const unsigned char *stage,
+                                          const float *apet, int c, int g, bool first, ChunkState &cs)
 {
 #pragma unroll
     for (int i = 0; i < kKC; ++i) {
-        if (!pos_valid<COFF>(c, i, first))
-            continue;
         int part, tok;
-        position<COFF>(c, i, part, tok);
-        const int off = tok * Geo<COFF>::TC * 2 + 8 * g;
-        const uint2 sw = *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(1, part) + off);
-        const float4 av =
-            *reinterpret_cast<const float4 *>(apet + (size_t)(c + Geo<COFF>::NC * i) * Geo<COFF>::TC + 4 * g);
+        if (!w.pos(c, i, part, tok) || (COFF == 2 && part == 0 && first))
+            continue;
+        const int off = tok * Geo<COFF, NCB>::TC * 2 + 8 * g;
+        const uint2 sw = *reinterpret_cast<const uint2 *>(stage + w.box_offset(1, part) + off);
+        const float4 av = *reinterpret_cast<const float4 *>(apet + (size_t)(c + NCB * i) * Geo<COFF, NCB>::TC + 4 * g);
         // unpacked and added as a pair: here measured faster than the mixed-precision
-        // add of r128_load (272 against 281 us for the coff-2 backward; same bits)
+        // add of ch_load (272 against 281 us for the ratio-128 coff-2 backward; same bits)
         cs.e[i][0] = add2(bf16x2_to_f2(sw.x), make_float2(av.x, av.y));
         cs.e[i][1] = add2(bf16x2_to_f2(sw.y), make_float2(av.z, av.w));
     }
@@ -290,13 +314,14 @@ __device__ __forceinline__ void r128_load_s(const unsigned char *stage, const fl
 
 // kv words of window position i of the thread: from the registers the forward
 // filled, or (KV_STAGE, the backward) from the stage.
-template <int COFF, bool KV_STAGE>
-__device__ __forceinline__ uint2 r128_kv(const ChunkState &cs, const unsigned char *stage, int c, int g, int i)
+template <int COFF, int NCB, int RC, bool KV_STAGE>
+__device__ __forceinline__ uint2 ch_kv(const Win<COFF, NCB, RC> &w, const ChunkState &cs, const unsigned char *stage,
+                                       int c, int g, int i)
 {
     if constexpr (KV_STAGE) {
         int part, tok;
-        position<COFF>(c, i, part, tok);
-        return *reinterpret_cast<const uint2 *>(stage + box_offset<COFF>(0, part) + tok * Geo<COFF>::TC * 2 + 8 * g);
+        w.pos(c, i, part, tok);
+        return *reinterpret_cast<const uint2 *>(stage + w.box_offset(0, part) + tok * Geo<COFF, NCB>::TC * 2 + 8 * g);
     } else {
         return cs.kv[i];
     }
@@ -307,18 +332,19 @@ __device__ __forceinline__ uint2 r128_kv(const ChunkState &cs, const unsigned ch
 // data succeeded): if any thread failed, all return false together before the
 // second barrier.  `have`: the row has data (cs loaded).  On true: cs.e holds e_k
 // of the thread's valid positions, and each warp's sums over its chunks are in
-// the merge buffers for r128_final.
-template <int COFF, bool KV_STAGE>
-__device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int c, int g, bool ok, bool have,
-                                          bool first, ChunkState &cs, const unsigned char *stage)
+// the merge buffers for ch_final.
+template <int COFF, int NCB, int RC, bool KV_STAGE>
+__device__ __forceinline__ bool ch_pool(const Win<COFF, NCB, RC> &w, const ChSmem<COFF, NCB> &s, int buf, int c,
+                                        int g, bool ok, bool have, bool first, ChunkState &cs,
+                                        const unsigned char *stage)
 {
-    using G = Geo<COFF>;
+    using G = Geo<COFF, NCB>;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
     if (have) {
 #pragma unroll
         for (int i = 0; i < kKC; ++i) {
-            if (!pos_valid<COFF>(c, i, first))
+            if (!w.valid(c, i, first))
                 continue;
             m[0] = max_nan(m[0], cs.e[i][0].x);
             m[1] = max_nan(m[1], cs.e[i][0].y);
@@ -339,12 +365,12 @@ __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int 
         return false;
     float4 M = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
-    for (int w = 0; w < G::CW; ++w) {
-        const float4 v = *reinterpret_cast<const float4 *>(mx + w * G::RS + 4 * g);
-        M.x = max_nan(M.x, v.x);
-        M.y = max_nan(M.y, v.y);
-        M.z = max_nan(M.z, v.z);
-        M.w = max_nan(M.w, v.w);
+    for (int v = 0; v < G::CW; ++v) {
+        const float4 x = *reinterpret_cast<const float4 *>(mx + v * G::RS + 4 * g);
+        M.x = max_nan(M.x, x.x);
+        M.y = max_nan(M.y, x.y);
+        M.z = max_nan(M.z, x.z);
+        M.w = max_nan(M.w, x.w);
     }
     float2 den[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
     float2 num[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
@@ -353,9 +379,9 @@ __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int 
                            make_float2(-__fmul_rn(M.z, kLog2eF), -__fmul_rn(M.w, kLog2eF))};
 #pragma unroll
     for (int i = 0; i < kKC; ++i) {
-        if (!have || !pos_valid<COFF>(c, i, first))
+        if (!have || !w.valid(c, i, first))
             continue;
-        const uint2 kv = r128_kv<COFF, KV_STAGE>(cs, stage, c, g, i);
+        const uint2 kv = ch_kv<COFF, NCB, RC, KV_STAGE>(w, cs, stage, c, g, i);
         const uint32_t kw[2] = {kv.x, kv.y};
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -387,14 +413,14 @@ __device__ __forceinline__ bool r128_pool(const R128Smem<COFF> &s, int buf, int 
     return true;
 }
 
-// The fixed-order merge of the eight warp sums, spread over all consumer threads:
-// TPC consecutive threads own tile column j; each adds its warps' sums in
-// ascending order, then the TPC partial sums meet in a fixed xor-shuffle tree, so
-// every one of them ends with the same den and num of column j.
-template <int COFF>
-__device__ __forceinline__ void r128_final(const R128Smem<COFF> &s, int buf, int &j, float &den, float &num)
+// The fixed-order merge of the warp sums, spread over all consumer threads: TPC
+// consecutive threads own tile column j; each adds its warps' sums in ascending
+// order, then the TPC partial sums meet in a fixed xor-shuffle tree, so every one
+// of them ends with the same den and num of column j.
+template <int COFF, int NCB>
+__device__ __forceinline__ void ch_final(const ChSmem<COFF, NCB> &s, int buf, int &j, float &den, float &num)
 {
-    using G = Geo<COFF>;
+    using G = Geo<COFF, NCB>;
     constexpr int TPC = G::CT / G::TC;  // threads per column
     constexpr int WPT = G::CW / TPC;    // warp sums per thread
     static_assert(TPC * G::TC == G::CT && WPT * TPC == G::CW, "merge split");
@@ -405,9 +431,9 @@ __device__ __forceinline__ void r128_final(const R128Smem<COFF> &s, int buf, int
     den = dn[0];
     num = nm[0];
 #pragma unroll
-    for (int w = 1; w < WPT; ++w) {
-        den = __fadd_rn(den, dn[w * G::RS]);
-        num = __fadd_rn(num, nm[w * G::RS]);
+    for (int v = 1; v < WPT; ++v) {
+        den = __fadd_rn(den, dn[v * G::RS]);
+        num = __fadd_rn(num, nm[v * G::RS]);
     }
 #pragma unroll
     for (int d = 1; d < TPC; d *= 2) {
@@ -421,7 +447,7 @@ __device__ __forceinline__ void r128_final(const R128Smem<COFF> &s, int buf, int
 // shared array, so the compiler keeps shared-memory addressing for every pointer
 // derived from it -- faster in the forwards and the lean backward.  Otherwise
 // through an integer round trip, which the register-resident coff-1 backward
-// measured faster with (it then fits its 168 registers without a spill).
+// measured faster with (it then fits its registers without a spill).
 template <bool OFFSET>
 __device__ __forceinline__ unsigned char *align_1k(unsigned char *raw)
 {
@@ -431,10 +457,10 @@ __device__ __forceinline__ unsigned char *align_1k(unsigned char *raw)
         return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
 
-template <int COFF>
-__device__ __forceinline__ void r128_init(const R128Smem<COFF> &s, int stages)
+template <int COFF, int NCB>
+__device__ __forceinline__ void ch_init(const ChSmem<COFF, NCB> &s, int stages)
 {
-    using G = Geo<COFF>;
+    using G = Geo<COFF, NCB>;
     if (threadIdx.x == 0) {
         for (int i = 0; i < stages; ++i) {
             mbar_init(smem_addr(&s.full[i]), 1);
@@ -447,28 +473,29 @@ __device__ __forceinline__ void r128_init(const R128Smem<COFF> &s, int stages)
 
 // ------------------------------------------------------------------ forward
 
-template <int COFF>
-__global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
-    fwd_r128_kernel(R128Args a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
-                    uint16_t *__restrict__ out)
+template <int COFF, int NCB, int RC>
+__global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, 2)
+    fwd_chunk_kernel(ChArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                     uint16_t *__restrict__ out)
 {
-    using G = Geo<COFF>;
+    using G = Geo<COFF, NCB>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem_base = align_1k<true>(smem_raw);
-    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes, false);
+    const ChSmem<COFF, NCB> s = ch_carve<COFF, NCB>(smem_base, a.stages, a.stage_bytes, false);
+    const Win<COFF, NCB, RC> w(a);
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    r128_init<COFF>(s, a.stages);
+    ch_init<COFF, NCB>(s, a.stages);
     pdl_wait();
     pdl_trigger();
     if (warp == G::CW) {
         if (lane == 0)
-            r128_produce<COFF, false>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
+            ch_produce<COFF, NCB, RC, false>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, a.capacity, nullptr);
         return;
     }
     const int g = lane % G::G, c = G::CPW * warp + lane / G::G;
     float2 ap[kKC][2];
-    r128_load_ape<COFF>(a, c, c0 + 4 * g, ap);
+    ch_load_ape<COFF, NCB, RC>(a, w, c, c0 + 4 * g, ap);
     int st = 0, buf = 0;
     uint32_t ph = 0;
     for (int row = blockIdx.x; row < a.capacity; row += gridDim.x) {
@@ -476,7 +503,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
         const bool first = ok ? (bool)s.meta[st].first : true;
         ChunkState cs;
         if (ok)
-            r128_load<COFF>(s.stages + (size_t)st * a.stage_bytes, c, g, first, ap, cs);
+            ch_load<COFF, NCB, RC>(w, s.stages + (size_t)st * a.stage_bytes, c, g, first, ap, cs);
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
@@ -484,12 +511,12 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
             st = 0;
             ph ^= 1u;
         }
-        if (!r128_pool<COFF, false>(s, buf, c, g, ok, ok, first, cs, nullptr))
+        if (!ch_pool<COFF, NCB, RC, false>(w, s, buf, c, g, ok, ok, first, cs, nullptr))
             break;
         {
             int j;
             float den, num;
-            r128_final<COFF>(s, buf, j, den, num);
+            ch_final<COFF, NCB>(s, buf, j, den, num);
             if (threadIdx.x % (G::CT / G::TC) == 0) {
                 const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, recip_den(den)));
                 out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
@@ -503,13 +530,12 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, 2)
 
 // Zero tokens [t0, t1) in the thread's 4 columns (first half only, or all halves);
 // the chunks share the tokens: thread chunk c takes t0 + c, t0 + c + NC, ...
-template <int COFF>
-__device__ __forceinline__ void r128_zero_tokens(uint16_t *dkv, uint16_t *dscore, int64_t C, int head_dim,
-                                                 int col, int64_t t0, int64_t t1, int64_t n_tokens, int c,
-                                                 bool all_halves)
+template <int COFF, int NCB>
+__device__ __forceinline__ void ch_zero_tokens(uint16_t *dkv, uint16_t *dscore, int64_t C, int head_dim, int col,
+                                               int64_t t0, int64_t t1, int64_t n_tokens, int c, bool all_halves)
 {
     t1 = t1 < n_tokens ? t1 : n_tokens;
-    for (int64_t t = (t0 < 0 ? 0 : t0) + c; t < t1; t += Geo<COFF>::NC) {
+    for (int64_t t = (t0 < 0 ? 0 : t0) + c; t < t1; t += NCB) {
         *reinterpret_cast<uint2 *>(dkv + t * C + col) = make_uint2(0u, 0u);
         *reinterpret_cast<uint2 *>(dscore + t * C + col) = make_uint2(0u, 0u);
         if (COFF == 2 && all_halves) {
@@ -519,26 +545,28 @@ __device__ __forceinline__ void r128_zero_tokens(uint16_t *dkv, uint16_t *dscore
     }
 }
 
-template <int COFF>
-__global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
-    bwd_r128_kernel(R128Args a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
-                    int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
-                    uint16_t *__restrict__ dscore, float *__restrict__ partial)
+template <int COFF, int NCB, int RC>
+__global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF> ? 2 : 1)
+    bwd_chunk_kernel(ChArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                     int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
+                     uint16_t *__restrict__ dscore, float *__restrict__ partial)
 {
-    using G = Geo<COFF>;
+    using G = Geo<COFF, NCB>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     constexpr bool LEAN = kBwdLean<COFF>;
     unsigned char *smem_base = align_1k<LEAN>(smem_raw);
-    const R128Smem<COFF> s = r128_carve<COFF>(smem_base, a.stages, a.stage_bytes, LEAN);
+    const ChSmem<COFF, NCB> s = ch_carve<COFF, NCB>(smem_base, a.stages, a.stage_bytes, LEAN);
+    const Win<COFF, NCB, RC> w(a);
+    const int R = w.ratio();
     const int c0 = blockIdx.y * G::TC;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t C = (int64_t)COFF * a.head_dim;
-    r128_init<COFF>(s, a.stages);
+    ch_init<COFF, NCB>(s, a.stages);
     pdl_wait();
     pdl_trigger();  // the grad_ape finalisation may launch; it waits for this grid's end
-    const int R = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;
+    const int Rr = a.n_seg > 0 ? __ldg(a.cc + a.n_seg) : 0;  // real rows
     const int R0 = a.n_seg > 0 ? __ldg(a.cc) : 0;
-    const int rend = R < a.capacity ? R : a.capacity;
+    const int rend = Rr < a.capacity ? Rr : a.capacity;
     const int64_t n_tokens = n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg);
 
     const int g = lane % G::G, c = G::CPW * warp + lane / G::G;
@@ -550,26 +578,27 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
 
     if (warp == G::CW) {
         if (lane == 0)
-            r128_produce<COFF, true>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, rend, grad_out);
+            ch_produce<COFF, NCB, RC, true>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, rend, grad_out);
     } else {
         if (blockIdx.x == 0) {  // leading gap: tokens before the first real block
             int64_t lead = n_tokens;
-            if (R0 < R)
-                lead = map_row(R0, a.cu, a.cc, a.n_seg, kR).base;
-            r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, 0, lead, n_tokens, c, true);
+            if (R0 < Rr)
+                lead = map_row(R0, a.cu, a.cc, a.n_seg, R).base;
+            ch_zero_tokens<COFF, NCB>(dkv, dscore, C, a.head_dim, col, 0, lead, n_tokens, c, true);
         }
         float2 ap[kKC][2];
         if constexpr (LEAN) {
             // the block's APE tile [window position][tile column], read once
-            for (int v = threadIdx.x; v < G::W * G::TC / 4; v += G::CT) {
+            const int W = COFF * R;
+            for (int v = threadIdx.x; v < W * G::TC / 4; v += G::CT) {
                 const int k = v / (G::TC / 4), c4 = v - k * (G::TC / 4);
-                const int part = k / kR, tk = k - part * kR;
+                const int part = k / R, tk = k - part * R;
                 *reinterpret_cast<float4 *>(s.apet + (size_t)v * 4) = __ldg(reinterpret_cast<const float4 *>(
                     a.ape + (int64_t)tk * C + (int64_t)part * a.head_dim + c0 + 4 * c4));
             }
             named_barrier(1, G::CT);
         } else {
-            r128_load_ape<COFF>(a, c, col, ap);
+            ch_load_ape<COFF, NCB, RC>(a, w, c, col, ap);
         }
         int st = 0, buf = 0;
         uint32_t ph = 0;
@@ -585,13 +614,13 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
             ChunkState cs;
             if (ok && m.real) {
                 if constexpr (LEAN)
-                    r128_load_s<COFF>(stage, s.apet, c, g, first, cs);
+                    ch_load_s<COFF, NCB, RC>(w, stage, s.apet, c, g, first, cs);
                 else
-                    r128_load<COFF>(stage, c, g, first, ap, cs);
+                    ch_load<COFF, NCB, RC>(w, stage, c, g, first, ap, cs);
             }
             uint2 gw = make_uint2(0u, 0u);
             if (ok && m.real)
-                gw = *reinterpret_cast<const uint2 *>(stage + G::WIN_BYTES + 8 * g);
+                gw = *reinterpret_cast<const uint2 *>(stage + w.win_bytes() + 8 * g);
             if constexpr (!LEAN) {  // everything the row needs is in registers now
                 __syncwarp();
                 if (lane == 0)
@@ -602,7 +631,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
                 ph ^= 1u;
             }
             // lean: the stage stays held until the gradients below have read kv from it
-            if (!r128_pool<COFF, LEAN>(s, buf, c, g, ok, ok && m.real, first, cs, stage))
+            if (!ch_pool<COFF, NCB, RC, LEAN>(w, s, buf, c, g, ok, ok && m.real, first, cs, stage))
                 break;
             const float2 gg[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
             const uint32_t gwq[2] = {gw.x, gw.y};
@@ -610,7 +639,7 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
             {
                 int j;
                 float den, num;
-                r128_final<COFF>(s, buf, j, den, num);
+                ch_final<COFF, NCB>(s, buf, j, den, num);
                 if (threadIdx.x % (G::CT / G::TC) == 0 && m.real) {
                     const float inv = recip_den(den);
                     fin[j] = inv;
@@ -633,17 +662,16 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
             const float2 go[2] = {mul2(gg[0], make_float2(o4.x, o4.y)), mul2(gg[1], make_float2(o4.z, o4.w))};
             const float2 ngo[2] = {make_float2(-go[0].x, -go[0].y), make_float2(-go[1].x, -go[1].y)};
             // window position k = c + NC*i sits at token t0 + k (part = k / ratio)
-            const int64_t t0 = m.base - (int64_t)(COFF - 1) * kR;
+            const int64_t t0 = m.base - (int64_t)(COFF - 1) * R;
             const int64_t lim = n_tokens - t0;  // positions k < lim hold a real token
             uint16_t *pk_dkv = dkv + t0 * C + (int64_t)c * C + col;
             uint16_t *pk_dsc = dscore + t0 * C + (int64_t)c * C + col;
 #pragma unroll
             for (int i = 0; i < kKC; ++i) {
-                if (!pos_valid<COFF>(c, i, first))
-                    continue;
                 int part, tk;
-                position<COFF>(c, i, part, tk);
-                const uint2 kv = r128_kv<COFF, LEAN>(cs, stage, c, g, i);
+                if (!w.pos(c, i, part, tk) || (COFF == 2 && part == 0 && first))
+                    continue;
+                const uint2 kv = ch_kv<COFF, NCB, RC, LEAN>(w, cs, stage, c, g, i);
                 const uint32_t kw[2] = {kv.x, kv.y};
                 uint32_t dk[2], dsw[2];
 #pragma unroll
@@ -654,8 +682,8 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
                     dsw[q] = f2_to_bf16x2(ds);
                     acc[i][q] = add2(acc[i][q], ds);
                 }
-                if (c + G::NC * i < lim) {
-                    const int64_t off = (int64_t)(G::NC * i) * C + (int64_t)part * a.head_dim;
+                if (c + NCB * i < lim) {
+                    const int64_t off = (int64_t)(NCB * i) * C + (int64_t)part * a.head_dim;
                     *reinterpret_cast<uint2 *>(pk_dkv + off) = make_uint2(dk[0], dk[1]);
                     *reinterpret_cast<uint2 *>(pk_dsc + off) = make_uint2(dsw[0], dsw[1]);
                 }
@@ -667,11 +695,11 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
             }
             if (m.last) {  // last block of its segment
                 if (COFF == 2)  // own block's first-half columns: read by no row
-                    r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, m.base, m.base + kR, n_tokens, c, false);
+                    ch_zero_tokens<COFF, NCB>(dkv, dscore, C, a.head_dim, col, m.base, m.base + R, n_tokens, c, false);
                 int64_t next = n_tokens;
-                if (m.row + 1 < R)
-                    next = map_row(m.row + 1, a.cu, a.cc, a.n_seg, kR).base;
-                r128_zero_tokens<COFF>(dkv, dscore, C, a.head_dim, col, m.base + kR, next, n_tokens, c, true);
+                if (m.row + 1 < Rr)
+                    next = map_row(m.row + 1, a.cu, a.cc, a.n_seg, R).base;
+                ch_zero_tokens<COFF, NCB>(dkv, dscore, C, a.head_dim, col, m.base + R, next, n_tokens, c, true);
             }
         }
     }
@@ -682,7 +710,8 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
 #pragma unroll
         for (int i = 0; i < kKC; ++i) {
             int part, tk;
-            position<COFF>(c, i, part, tk);
+            if (!w.pos(c, i, part, tk))
+                continue;
             *reinterpret_cast<float4 *>(red + (tk * COFF + part) * G::TC + 4 * g) =
                 make_float4(acc[i][0].x, acc[i][0].y, acc[i][1].x, acc[i][1].y);
         }
@@ -692,10 +721,10 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
     cluster.sync();
     const int rank = (int)cluster.block_rank();
     const int nrank = (int)cluster.num_blocks();
-    const int n4 = kR * COFF * G::TC / 4;
+    const int n4 = R * COFF * G::TC / 4;
     const int share = (n4 + nrank - 1) / nrank;
     const int lo = rank * share, hi = lo + share < n4 ? lo + share : n4;
-    float *dst = partial + (int64_t)(blockIdx.x / nrank) * kR * C;
+    float *dst = partial + (int64_t)(blockIdx.x / nrank) * R * C;
     for (int i4 = lo + (int)threadIdx.x; i4 < hi; i4 += blockDim.x) {
         const int rp = (i4 * 4) / G::TC, lcol = i4 * 4 - rp * G::TC;
         const int arow = rp / COFF, pp = rp - arow * COFF;
@@ -714,101 +743,46 @@ __global__ void __launch_bounds__(Geo<COFF>::THREADS, kBwdLean<COFF> ? 2 : 1)
 
 // ------------------------------------------------------------------- host
 
-// Tensor map of a [rows, C] bf16 row-major tensor with [128 x tc] boxes.
-cudaError_t make_map(CUtensorMap *m, const void *ptr, int64_t C, int tc)
-{
-    return make_tensor_map_2d(m, ptr, C, tc, kR);
-}
-
-struct R128Plan {
-    int stages, stage_bytes, threads, tiles, cluster;
+struct ChPlan {
+    int stages, stage_bytes, box_bytes, threads, tiles, cluster;
     size_t smem;
 };
 
-template <int COFF>
-R128Plan r128_plan(bool bwd, int head_dim)
+template <int COFF, int NCB>
+ChPlan ch_plan(bool bwd, int ratio, int head_dim)
 {
-    using G = Geo<COFF>;
-    R128Plan pl;
-    pl.stage_bytes = (G::WIN_BYTES + (bwd ? G::TC * 2 : 0) + 1023) / 1024 * 1024;
+    using G = Geo<COFF, NCB>;
+    ChPlan pl;
+    pl.box_bytes = (ratio * G::TC * 2 + 127) / 128 * 128;
+    pl.stage_bytes = (2 * COFF * pl.box_bytes + (bwd ? G::TC * 2 : 0) + 1023) / 1024 * 1024;
     const bool tile = bwd && kBwdLean<COFF>;
     // two blocks per SM (forward, lean backward): two stages; one block per SM
     // (register-resident backward): a four-stage ring fits
     pl.stages = bwd && !tile ? 4 : 2;
     pl.threads = G::THREADS;
     pl.tiles = head_dim / G::TC;
-    // no clusters for the lean backward: pairs of blocks would halve the grad_ape
-    // partials, but the grid must then be an even number of blocks per column
-    // tile, which leaves SMs idle (19 blocks per tile fill 152 SMs twice over at
-    // head_dim 512)
-    pl.cluster = bwd ? (tile ? 1 : CSA_R128_BWD_CLUSTER) : 1;
-    pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes, tile) + 1024;  // + alignment slack
+    // no clusters: pairs of blocks would halve the grad_ape partials, but the grid
+    // must then be an even number of blocks per column tile, which leaves SMs idle
+    // (19 blocks per tile fill 152 SMs twice over at head_dim 512, coff 2)
+    pl.cluster = 1;
+    pl.smem = ch_smem_bytes<COFF, NCB>(pl.stages, pl.stage_bytes, tile) + 1024;  // + alignment slack
     if (bwd) {  // grad_ape staging reuses the stages: make sure it fits
-        const size_t red = (size_t)kR * COFF * G::TC * sizeof(float);
+        const size_t red = (size_t)ratio * COFF * G::TC * sizeof(float);
         if ((size_t)pl.stages * pl.stage_bytes < red)
             pl.stages = (int)((red + pl.stage_bytes - 1) / pl.stage_bytes);
-        pl.smem = r128_smem_bytes<COFF>(pl.stages, pl.stage_bytes, tile) + 1024;
+        pl.smem = ch_smem_bytes<COFF, NCB>(pl.stages, pl.stage_bytes, tile) + 1024;
     }
     return pl;
 }
 
-template <int COFF>
-cudaError_t r128_blocks(const R128Plan &pl, bool bwd, int rows, int *out)
+// Row blocks per column tile: as many as are resident on the device, at most one
+// per row.
+cudaError_t ch_blocks(const void *fn, const ChPlan &pl, int rows, int *out)
 {
-    const void *fn = bwd ? reinterpret_cast<const void *>(bwd_r128_kernel<COFF>)
-                         : reinterpret_cast<const void *>(fwd_r128_kernel<COFF>);
-    static std::mutex mu;
-    static int cache_dev[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
-    static int cache_val[8];
-    static const void *cache_fn[8];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    int resident = 0;
+    cudaError_t e = resident_blocks(fn, pl.threads, pl.smem, pl.cluster, &resident);
     if (e != cudaSuccess)
         return e;
-    int resident = -1;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        for (int i = 0; i < 8; ++i)
-            if (cache_dev[i] == dev && cache_fn[i] == fn)
-                resident = cache_val[i];
-    }
-    if (resident < 0) {
-        e = allow_max_smem(fn);  // the function-wide limit: the device maximum, whatever this plan needs
-        if (e != cudaSuccess)
-            return e;
-        if (pl.cluster > 1) {
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(pl.cluster, 1, 1);
-            cfg.blockDim = dim3(pl.threads, 1, 1);
-            cfg.dynamicSmemBytes = pl.smem;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = pl.cluster;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg);
-            resident = clusters * pl.cluster;
-        } else {
-            int per_sm = 0, sms = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, pl.threads, pl.smem);
-            if (e == cudaSuccess)
-                e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            resident = per_sm * sms;
-        }
-        if (e != cudaSuccess)
-            return e;
-        std::lock_guard<std::mutex> lk(mu);
-        for (int i = 0; i < 8; ++i)
-            if (cache_dev[i] < 0) {
-                cache_dev[i] = dev;
-                cache_fn[i] = fn;
-                cache_val[i] = resident;
-                break;
-            }
-    }
     int blocks = (resident > 0 ? resident : 1) / pl.tiles;
     blocks = blocks / pl.cluster * pl.cluster;
     if (blocks < pl.cluster)
@@ -820,21 +794,29 @@ cudaError_t r128_blocks(const R128Plan &pl, bool bwd, int rows, int *out)
     return cudaSuccess;
 }
 
-template <int COFF>
-cudaError_t launch_fwd_r128_t(const FwdParams &p, unsigned *status, cudaStream_t st)
+ChArgs ch_args(const void *kv, const void *score, const float *ape, const int32_t *cu, const int32_t *cc, int n_seg,
+               int head_dim, int capacity, int ratio, const ChPlan &pl, unsigned *status)
 {
-    const R128Plan pl = r128_plan<COFF>(false, p.head_dim);
+    return ChArgs{static_cast<const uint16_t *>(kv), static_cast<const uint16_t *>(score), ape, cu, cc, n_seg,
+                  head_dim, capacity, ratio, pl.box_bytes, pl.stages, pl.stage_bytes, status};
+}
+
+template <int COFF, int NCB, int RC>
+cudaError_t launch_fwd_ch(const FwdParams &p, unsigned *status, cudaStream_t st)
+{
+    const ChPlan pl = ch_plan<COFF, NCB>(false, p.ratio, p.head_dim);
+    auto kern = fwd_chunk_kernel<COFF, NCB, RC>;
     int blocks = 0;
-    cudaError_t e = r128_blocks<COFF>(pl, false, p.capacity, &blocks);
+    cudaError_t e = ch_blocks(reinterpret_cast<const void *>(kern), pl, p.capacity, &blocks);
     if (e != cudaSuccess)
         return e;
     CUtensorMap mk, ms;
     const int64_t C = (int64_t)COFF * p.head_dim;
-    if ((e = make_map(&mk, p.kv, C, Geo<COFF>::TC)) != cudaSuccess ||
-        (e = make_map(&ms, p.score, C, Geo<COFF>::TC)) != cudaSuccess)
+    if ((e = make_tensor_map_2d(&mk, p.kv, C, Geo<COFF, NCB>::TC, p.ratio)) != cudaSuccess ||
+        (e = make_tensor_map_2d(&ms, p.score, C, Geo<COFF, NCB>::TC, p.ratio)) != cudaSuccess)
         return e;
-    R128Args a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
-               p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes, status};
+    const ChArgs a = ch_args(p.kv, p.score, p.ape, p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity,
+                             p.ratio, pl, status);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks, pl.tiles, 1);
     cfg.blockDim = dim3(pl.threads, 1, 1);
@@ -843,28 +825,31 @@ cudaError_t launch_fwd_r128_t(const FwdParams &p, unsigned *status, cudaStream_t
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_r128_kernel<COFF>, a, mk, ms, static_cast<uint16_t *>(p.out));
+    return cudaLaunchKernelEx(&cfg, kern, a, mk, ms, static_cast<uint16_t *>(p.out));
 }
 
-template <int COFF>
-cudaError_t r128_bwd_blocks_t(int head_dim, int capacity, int *blocks)
+template <int COFF, int NCB, int RC>
+cudaError_t ch_bwd_blocks(int ratio, int head_dim, int capacity, int *blocks, int *cluster)
 {
-    const R128Plan pl = r128_plan<COFF>(true, head_dim);
-    return r128_blocks<COFF>(pl, true, capacity, blocks);
+    const ChPlan pl = ch_plan<COFF, NCB>(true, ratio, head_dim);
+    *cluster = pl.cluster;
+    return ch_blocks(reinterpret_cast<const void *>(bwd_chunk_kernel<COFF, NCB, RC>), pl, capacity, blocks);
 }
 
-template <int COFF>
-cudaError_t launch_bwd_r128_t(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st)
+template <int COFF, int NCB, int RC>
+cudaError_t launch_bwd_ch(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st)
 {
-    const R128Plan pl = r128_plan<COFF>(true, p.head_dim);
+    const ChPlan pl = ch_plan<COFF, NCB>(true, p.ratio, p.head_dim);
+    auto kern = bwd_chunk_kernel<COFF, NCB, RC>;
     CUtensorMap mk, ms;
     const int64_t C = (int64_t)COFF * p.head_dim;
     cudaError_t e;
-    if ((e = make_map(&mk, p.kv, C, Geo<COFF>::TC)) != cudaSuccess ||
-        (e = make_map(&ms, p.score, C, Geo<COFF>::TC)) != cudaSuccess)
+    if ((e = allow_max_smem(reinterpret_cast<const void *>(kern))) != cudaSuccess ||
+        (e = make_tensor_map_2d(&mk, p.kv, C, Geo<COFF, NCB>::TC, p.ratio)) != cudaSuccess ||
+        (e = make_tensor_map_2d(&ms, p.score, C, Geo<COFF, NCB>::TC, p.ratio)) != cudaSuccess)
         return e;
-    R128Args a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape, p.cu_seqlens,
-               p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes, status};
+    const ChArgs a = ch_args(p.kv, p.score, p.ape, p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity,
+                             p.ratio, pl, status);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks, pl.tiles, 1);
     cfg.blockDim = dim3(pl.threads, 1, 1);
@@ -878,41 +863,56 @@ cudaError_t launch_bwd_r128_t(const BwdParams &p, float *partial, int blocks, un
     attr[1] = pdl_attribute();
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, bwd_r128_kernel<COFF>, a, mk, ms, p.n_tokens,
-                           static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
-                           static_cast<uint16_t *>(p.dscore), partial);
+    e = cudaLaunchKernelEx(&cfg, kern, a, mk, ms, p.n_tokens, static_cast<const uint16_t *>(p.grad_out),
+                           static_cast<uint16_t *>(p.dkv), static_cast<uint16_t *>(p.dscore), partial);
     if (e != cudaSuccess)
         return e;
-    return launch_dape_finalize(partial, blocks / pl.cluster, (int64_t)kR * C, p.dape, st);
+    return launch_dape_finalize(partial, blocks / pl.cluster, (int64_t)p.ratio * C, p.dape, st);
 }
 
 }  // namespace
 
-bool r128_supported(int ratio, int coff, int head_dim)
+bool chunked_supported(int ratio, int coff, int head_dim)
 {
-    return ratio == kR && (coff == 1 || coff == 2) && head_dim % 64 == 0 && head_dim <= 8192;
+    if (head_dim % 64 != 0 || head_dim < 64 || head_dim > 8192 || ratio > 128)
+        return false;
+    return (coff == 1 && ratio > 64) || (coff == 2 && ratio > 32);
 }
 
-cudaError_t launch_fwd_r128(const FwdParams &p, unsigned *status, cudaStream_t st)
+// The kernel instance for a shape: ratio 128 with the ratio as a constant (16
+// chunks for coff 1, 32 for coff 2); other ratios at run time, 16 chunks for
+// windows of up to 128 positions, 32 up to 256.
+#define CSA_CHUNK_DISPATCH(FN, ...)                                                         \
+    do {                                                                                    \
+        if (ratio == 128)                                                                   \
+            return coff == 2 ? FN<2, 32, 128>(__VA_ARGS__) : FN<1, 16, 128>(__VA_ARGS__);   \
+        if (coff == 1)                                                                      \
+            return FN<1, 16, 0>(__VA_ARGS__);                                               \
+        return 2 * ratio <= 128 ? FN<2, 16, 0>(__VA_ARGS__) : FN<2, 32, 0>(__VA_ARGS__);    \
+    } while (0)
+
+cudaError_t launch_fwd_chunked(const FwdParams &p, unsigned *status, cudaStream_t st)
 {
-    return p.coff == 2 ? launch_fwd_r128_t<2>(p, status, st) : launch_fwd_r128_t<1>(p, status, st);
+    const int ratio = p.ratio, coff = p.coff;
+    CSA_CHUNK_DISPATCH(launch_fwd_ch, p, status, st);
 }
 
-// grad_ape partials the backward will write (the workspace needs that many
-// ratio x coff*head_dim slabs); also the grid width it will use.
-cudaError_t r128_bwd_partials(int coff, int head_dim, int capacity, int *partials, int *blocks)
+// Grid width of the backward and the number of grad_ape partials it writes (the
+// workspace needs that many ratio x coff*head_dim slabs).
+cudaError_t chunked_bwd_partials(int ratio, int coff, int head_dim, int capacity, int *partials, int *blocks)
 {
-    cudaError_t e = coff == 2 ? r128_bwd_blocks_t<2>(head_dim, capacity, blocks)
-                              : r128_bwd_blocks_t<1>(head_dim, capacity, blocks);
-    const int cluster = coff == 2 ? r128_plan<2>(true, head_dim).cluster : r128_plan<1>(true, head_dim).cluster;
+    int cluster = 1;
+    cudaError_t e = [&]() -> cudaError_t { CSA_CHUNK_DISPATCH(ch_bwd_blocks, ratio, head_dim, capacity, blocks, &cluster); }();
     *partials = *blocks / cluster;
     return e;
 }
 
-cudaError_t launch_bwd_r128(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st)
+cudaError_t launch_bwd_chunked(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st)
 {
-    return p.coff == 2 ? launch_bwd_r128_t<2>(p, partial, blocks, status, st)
-                       : launch_bwd_r128_t<1>(p, partial, blocks, status, st);
+    const int ratio = p.ratio, coff = p.coff;
+    CSA_CHUNK_DISPATCH(launch_bwd_ch, p, partial, blocks, status, st);
 }
+
+#undef CSA_CHUNK_DISPATCH
 
 }  // namespace csa

@@ -93,15 +93,17 @@ cudaError_t launch_bwd_stream(const BwdParams &p, const StreamPlan &pl, float *p
 // The exact grid width launch_bwd_stream uses (partials = blocks / pl.cluster).
 cudaError_t stream_bwd_blocks(int ratio, int coff, const StreamPlan &pl, int capacity, int *blocks);
 
-// Ratio-128 family (chunked window, 2-D TMA staging), head_dim % 64 == 0.
-bool r128_supported(int ratio, int coff, int head_dim);
-cudaError_t launch_fwd_r128(const FwdParams &p, unsigned *status, cudaStream_t st);
+// Chunked family (windows of more than 64 positions: ratio 128, and ratios 33-127
+// with coff 2 / 65-127 with coff 1; 2-D TMA staging), head_dim % 64 == 0.
+bool chunked_supported(int ratio, int coff, int head_dim);
+cudaError_t launch_fwd_chunked(const FwdParams &p, unsigned *status, cudaStream_t st);
 // grid width of the backward and the number of grad_ape partials it writes
-cudaError_t r128_bwd_partials(int coff, int head_dim, int capacity, int *partials, int *blocks);
-cudaError_t launch_bwd_r128(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st);
+cudaError_t chunked_bwd_partials(int ratio, int coff, int head_dim, int capacity, int *partials, int *blocks);
+cudaError_t launch_bwd_chunked(const BwdParams &p, float *partial, int blocks, unsigned *status, cudaStream_t st);
 
-// Every other ratio in [1, 128] (thread per column pair, window walked from global
-// memory), head_dim % 8 == 0.
+// Every other shape of a ratio other than 4 and 128 (windows of up to 64 positions
+// staged in shared memory, head_dim % 64 == 0; else a thread per column pair walking
+// the window from global memory), head_dim % 8 == 0.
 struct GenericPlan {
     int col_tiles;          // blocks along the columns (16 groups of 4 columns each)
     int lanes;              // rows walked side by side in a block (blockDim.y)
@@ -136,14 +138,14 @@ cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int b
 // The backward's kernel family and plan for one shape on the current device: one
 // computation shared by csa_compress_bwd, csa_compress_bwd_noalloc and
 // csa_grad_ape_order, so that the reported grad_ape grouping is the launched one.
-enum BwdFamily { kBwdR128 = 0, kBwdGeneric = 1, kBwdStream = 2, kBwdSmall = 3 };
+enum BwdFamily { kBwdChunked = 0, kBwdGeneric = 1, kBwdStream = 2, kBwdSmall = 3 };
 struct BwdPlan {
     BwdFamily family;
     StreamPlan sp;
     SmallBwdPlan pl;
     GenericPlan gp;
-    int r128_blocks;     // ratio 128: grid width
-    int r128_partials;   // ratio 128: grad_ape partials
+    int ch_blocks;       // chunked: grid width (row blocks per column tile)
+    int ch_partials;     // chunked: grad_ape partials
     int stream_blocks;   // streamed: exact grid width (row blocks per column tile)
     int64_t floats;      // grad_ape partial floats the launch needs (an upper bound)
 };

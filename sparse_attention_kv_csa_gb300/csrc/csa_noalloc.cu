@@ -131,14 +131,14 @@ extern "C" int csa_compress_bwd_noalloc(const void *kv, const void *score, const
         return csa::fail_status(CSA_ERR_CUDA, "no-alloc plan: %s", cudaGetErrorString(e));
     int64_t floats = plan.floats;
     const int64_t per = (int64_t)ratio * coff * head_dim;
-    if (plan.family == csa::kBwdR128 && floats > (int64_t)kScratchFloats && per <= (int64_t)kScratchFloats &&
-        plan.r128_partials > 0) {
+    if (plan.family == csa::kBwdChunked && floats > (int64_t)kScratchFloats && per <= (int64_t)kScratchFloats &&
+        plan.ch_partials > 0) {
         // More partials than the array holds: fewer row blocks per column tile
         // (each walks more rows; one partial per cluster of blocks).
-        const int cluster = plan.r128_blocks / plan.r128_partials;
+        const int cluster = plan.ch_blocks / plan.ch_partials;
         const int fit = (int)((int64_t)kScratchFloats / per);
-        plan.r128_blocks = fit * cluster;
-        plan.r128_partials = fit;
+        plan.ch_blocks = fit * cluster;
+        plan.ch_partials = fit;
         floats = (int64_t)fit * per;
     } else if (plan.family == csa::kBwdStream) {
         // the exact grid's partials (the regular call sizes its pool block by an upper bound)

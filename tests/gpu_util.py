@@ -3,6 +3,7 @@ points with NaN-canary prefilled outputs, download, compare."""
 import numpy as np
 
 import csa_workloads as w
+import oracle
 
 F = w.bf16_bits_to_f32
 CANARY_BF16 = 0xFFFF  # a NaN pattern: any slot the kernel fails to write stays NaN
@@ -88,7 +89,6 @@ def check_dape(c, dape, csa, grouping=None):
     (csa_grad_ape_order; the rows, leaves and combination are formed by the oracle
     from the rules stated in include/csa.h).  Ratio 128 (chunked sums, tolerance
     contract): within 1e-5 (normwise) of the fp64 oracle.  Returns the grouping."""
-    import oracle
     g = grouping or csa.csa_grad_ape_order(c.ratio, c.coff, c.head_dim, c.capacity)
     if g["kind"] == "row_blocks":
         want = oracle.case_dape_grouped_f32(c, g)
@@ -100,3 +100,49 @@ def check_dape(c, dape, csa, grouping=None):
         _, _, d64 = oracle.case_bwd_f64(c)
         assert np.abs(dape - d64).max() <= 1e-5 * max(np.abs(d64).max(), 1e-30)
     return g
+
+
+# ------------------------------------------ chunked family (tolerance contract)
+
+def fp64_parity_ok(got_bits, ref32_bits, ref64):
+    """fp64-oracle parity ("CSA Fused Compressor", Numerics): the kernel is at least
+    as close to the fp64 oracle as the plain fp32 evaluation:
+    err_gpu <= err_fp32 * (1 + 1e-6) + 1e-4, err = max |bf16 value - fp64|."""
+    err_gpu = np.abs(F(got_bits).astype(np.float64) - ref64).max()
+    err_32 = np.abs(F(ref32_bits).astype(np.float64) - ref64).max()
+    return err_gpu <= err_32 * (1 + 1e-6) + 1e-4
+
+
+def tolerance_counts(c, csa, scale=1.0):
+    """The ratio-128 contract ("CSA Fused Compressor", Numerics: ratio == 128),
+    which the library applies to every window of more than 64 positions, per case: no NaN, max_abs <= 1.6e-2 against the plain fp32 and the fp64
+    oracle, fp64 parity no worse than the plain fp32 evaluation, never-consumed
+    slots exact zeros, grad_ape within 1e-5 (normwise) of fp64.  Returns the outputs and the
+    (differing-from-fp32, differing-from-fp64, size) counts of out / grad_kv /
+    grad_score, whose max(1, 0.1%) bound the callers apply."""
+    d = Dev(c)
+    out = run_fwd(d, csa)
+    dkv, dsc, dape = run_bwd(d, csa)
+    ref32 = (oracle.case_fwd_f32(c),) + tuple(oracle.case_bwd_f32(c))
+    ref64 = (oracle.case_fwd_f64(c),) + tuple(oracle.case_bwd_f64(c))
+    counts = []
+    for got, r32, r64, bound in ((out, ref32[0], ref64[0], 1.6e-2 * scale),
+                                 (dkv, ref32[1], ref64[1], 1.6e-2 * scale),
+                                 (dsc, ref32[2], ref64[2], 1.6e-2 * scale * scale)):
+        assert not np.isnan(F(got)).any()
+        assert np.abs(F(got).astype(np.float64) - F(r32)).max() <= bound
+        n64, max_abs = tolerance_report(got, r64)
+        assert max_abs <= bound
+        assert fp64_parity_ok(got, r32, r64)
+        counts.append((int((got != r32).sum()), n64, got.size))
+    owner = oracle.consumers(c.cu_seqlens, c.cu_seqlens_comp, c.ratio, c.coff, c.head_dim, c.capacity, c.n_tokens)
+    unread = owner == -1
+    assert not dkv[unread].any() and not dsc[unread].any()
+    assert np.abs(dape - ref64[3]).max() <= 1e-5 * np.abs(ref64[3]).max()
+    return (out, dkv, dsc, dape), counts
+
+
+def assert_counts(counts):
+    for n32, n64, size in counts:
+        assert n32 <= max(1, 0.001 * size), (n32, size)
+        assert n64 <= max(1, 0.001 * size), (n64, size)

@@ -1,5 +1,6 @@
-"""The generic-ratio kernels (every ratio in [1, 128] other than 4 and 128): the
-library's sequential fp32 order, so out / grad_kv / grad_score are bitwise equal to
+"""The generic-ratio kernels (every ratio in [1, 128] other than 4 and 128, except
+windows of more than 64 positions with head_dim a multiple of 64, which take the
+chunked kernels: test_gpu_chunked.py): the library's sequential fp32 order, so out / grad_kv / grad_score are bitwise equal to
 the fp32 oracle; grad_ape bitwise equal to the oracle's fp32 sum in the grouping
 the library reports (csa_grad_ape_order) and within 1e-5 (normwise) of the fp64
 oracle.  Ragged packs
@@ -29,6 +30,9 @@ def layout(ratio, i):
 
 
 def check(c, csa):
+    if csa.csa_grad_ape_order(c.ratio, c.coff, c.head_dim, c.capacity)["kind"] == "chunked":
+        pytest.skip("window of more than 64 positions with head_dim % 64 == 0: the chunked family, "
+                    "checked by tolerance in test_gpu_chunked.py")
     d = Dev(c)
     if c.capacity > 0:
         assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))
