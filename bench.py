@@ -64,6 +64,9 @@ def parse_args():
     p.add_argument("--min-warmup-seconds", type=float, default=1.0,
                    help="keep warming up at least this long (clock samples under load); 0 for profiling")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--pass-only", choices=["fwd", "bwd"],
+                   help="profiling aid: only K back-to-back calls of one pass after W warm-up calls; prints "
+                        "the mean time per call, not the benchmark line")
     return p.parse_args()
 
 
@@ -260,6 +263,12 @@ def run_ours(args, rank, world, local_rank):
     c = w.WORKLOADS[args.workload](seed=rank)
     stream = torch.cuda.current_stream()
     r = Resident(csa, c, dev, stream, world)
+    if args.pass_only:
+        fn = r.fwd if args.pass_only == "fwd" else r.bwd
+        for i in range(args.warmup):
+            fn(i)
+        ms = r.region(fn, args.steps)
+        return c, None, ms, None, None, None, {"pass_only": args.pass_only}
 
     sampler = ClockSampler(local_rank) if rank == 0 and not args.no_clocks else None
     if sampler:
@@ -503,6 +512,11 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     c, ms_step, ms_fwd, ms_bwd, clocks, e2e, extra = run_ours(args, rank, world, local_rank)
+    if args.pass_only:
+        if rank == 0:
+            print(json.dumps({"pass_only": args.pass_only, "workload": c.name, "calls": args.steps,
+                              "ms_per_call": ms_fwd}), flush=True)
+        return 0
     if rank != 0:
         if world > 1:
             import torch.distributed as dist

@@ -251,6 +251,13 @@ SPECS = {
                                             seqlens=[4096] * 8, extra_rows=16),
     "r96c1d512_8x6144": lambda seed=0: dict(name="r96c1d512_8x6144", ratio=96, coff=1, head_dim=512,
                                             seqlens=[6144] * 8),
+    # head_dims that are not multiples of 64: ratio 4 (register-window kernels,
+    # head_dim 96) and ratio 16 (the generic kernel that walks the window from
+    # global memory, head_dim 200)
+    "r4c2d96_32x4096": lambda seed=0: dict(name="r4c2d96_32x4096", ratio=4, coff=2, head_dim=96,
+                                           seqlens=[4096] * 32),
+    "r16c2d200_8x4096": lambda seed=0: dict(name="r16c2d200_8x4096", ratio=16, coff=2, head_dim=200,
+                                            seqlens=[4096] * 8),
 }
 
 

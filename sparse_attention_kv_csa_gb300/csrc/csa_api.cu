@@ -360,7 +360,7 @@ cudaError_t plan_bwd(int ratio, int coff, int head_dim, int capacity, int num_sm
         b.family = kBwdGeneric;
         e = plan_generic(ratio, coff, head_dim, capacity, num_sms, &b.gp);
         b.floats = b.gp.partial_floats;
-    } else if (stream_supported(ratio, coff, head_dim)) {
+    } else if (stream_supported(true, ratio, coff, head_dim)) {
         b.family = kBwdStream;
         b.sp = plan_stream(true, ratio, coff, head_dim, capacity, num_sms);
         e = stream_bwd_blocks(ratio, coff, b.sp, capacity, &b.stream_blocks);
@@ -446,7 +446,7 @@ int csa_compress_fwd(const void *kv, const void *score, const float *ape, const 
         e = csa::launch_fwd_chunked(p, ds->status, st);
     else if (ratio != 4)
         e = csa::launch_fwd_generic(p, ds->status, ds->num_sms, st);
-    else if (csa::stream_supported(ratio, coff, head_dim))
+    else if (csa::stream_supported(false, ratio, coff, head_dim))
         e = csa::launch_fwd_stream(p, csa::plan_stream(false, ratio, coff, head_dim, capacity, ds->num_sms),
                                    ds->status, st);
     else

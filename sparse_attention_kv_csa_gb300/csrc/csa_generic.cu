@@ -342,10 +342,7 @@ __global__ void __launch_bounds__(kGenBwdGroups * kGenBwdMaxLanes, 2)
 constexpr int kGsTile = 64;       // columns per block tile (two per consumer thread)
 constexpr int kGsMaxWindow = 64;  // coff * ratio
 constexpr int kGsMaxLanes = 4;    // consumer warps per block
-#ifndef CSA_GS_BUDGET
-#define CSA_GS_BUDGET (64 * 1024)
-#endif
-constexpr int kGsRingBudget = CSA_GS_BUDGET;
+constexpr int kGsRingBudget = 64 * 1024;  // ring bytes of a block with four consumer warps
 constexpr size_t kGsSmemPerSM = 228 * 1024;  // shared memory per SM, 1 KB of it reserved per block
 
 struct GsArgs {

@@ -68,9 +68,11 @@ cudaError_t launch_fwd_small(const FwdParams &p, int num_sms, cudaStream_t st);
 // grad_ape = fixed-order sum of n_partials partials of n floats each.
 cudaError_t launch_dape_finalize(const float *partial, int n_partials, int64_t n, float *dape, cudaStream_t st);
 
-// Streamed family (bulk-copy pipeline through shared memory), head_dim % 128 == 0.
+// Streamed family (bulk-copy pipeline through shared memory), ratio 4,
+// head_dim % 64 == 0.
 struct StreamPlan {
-    int tc;              // columns per thread block tile (consumer threads x 4)
+    int np;              // fp32 column pairs per consumer thread: 2 (head_dim % 128 == 0) or 1
+    int tc;              // columns per thread block tile (consumer threads x 2 np)
     int tiles;           // head_dim / tc (gridDim.y)
     int row_lanes;       // rows in flight per block (tc / 128 column warps each)
     bool whole;          // stage whole token rows (one column tile)
@@ -84,7 +86,7 @@ struct StreamPlan {
     int num_sms;
 };
 
-bool stream_supported(int ratio, int coff, int head_dim);
+bool stream_supported(bool bwd, int ratio, int coff, int head_dim);
 StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity, int num_sms);
 int stream_bwd_partials(const StreamPlan &pl, int capacity);
 cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st);

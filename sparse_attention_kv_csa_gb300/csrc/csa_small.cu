@@ -217,15 +217,10 @@ __device__ __forceinline__ void pool_window(const SmallArgs &a, const RowMap &rm
 
 // -------------------------------------------------------------- forward
 
-// Tile choices (compile-time): words of bf16 per window row per thread and the
-// minimum resident blocks per SM the register budget is sized for.
-#ifndef CSA_FWD_NW
-#define CSA_FWD_NW 2
-#endif
-#ifndef CSA_FWD_MINB
-#define CSA_FWD_MINB 3
-#endif
-constexpr int kFwdNW = CSA_FWD_NW;
+// Tile choices: words of bf16 per window row per thread and the minimum resident
+// blocks per SM the register budget is sized for.
+constexpr int kFwdNW = 2;
+constexpr int kFwdMinBlocks = 3;
 constexpr int kFwdThreads = 128;
 
 template <int RATIO, int COFF>
@@ -265,7 +260,7 @@ __device__ __forceinline__ void fwd_compute(const SmallArgs &a, const FwdUnit<RA
 // buffers alternate: the next unit's loads are issued before the current one is
 // computed.
 template <int RATIO, int COFF>
-__global__ void __launch_bounds__(kFwdThreads, CSA_FWD_MINB) fwd_small_kernel(SmallArgs a, uint16_t *__restrict__ out)
+__global__ void __launch_bounds__(kFwdThreads, kFwdMinBlocks) fwd_small_kernel(SmallArgs a, uint16_t *__restrict__ out)
 {
     pdl_wait();
     pdl_trigger();
@@ -297,16 +292,9 @@ __global__ void __launch_bounds__(kFwdThreads, CSA_FWD_MINB) fwd_small_kernel(Sm
 
 // ------------------------------------------------------------- backward
 
-#ifndef CSA_BWD_NW
-#define CSA_BWD_NW 1
-#endif
-#ifndef CSA_BWD_MINB
-#define CSA_BWD_MINB 4
-#endif
-#ifndef CSA_BWD_CLUSTER
-#define CSA_BWD_CLUSTER 4
-#endif
-constexpr int kBwdNW = CSA_BWD_NW;
+constexpr int kBwdNW = 1;
+constexpr int kBwdMinBlocks = 4;  // resident blocks per SM the register budget is sized for
+constexpr int kBwdCluster = 4;    // blocks per cluster (grad_ape merged in DSMEM)
 constexpr int kBwdThreads = 128;
 
 template <int RATIO, int COFF>
@@ -428,7 +416,7 @@ __device__ __forceinline__ void bwd_compute(const SmallArgs &a, const BwdRow<RAT
 // threads of row 0 zero the tokens before the first real block.  Every token of
 // [0, n_tokens) is thus written exactly once.
 template <int RATIO, int COFF>
-__global__ void __launch_bounds__(kBwdThreads, CSA_BWD_MINB)
+__global__ void __launch_bounds__(kBwdThreads, kBwdMinBlocks)
     bwd_small_kernel(SmallArgs a, int rows_per_block, int64_t n_tokens_arg,
                      const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
                      uint16_t *__restrict__ dscore, float *__restrict__ partial)
@@ -667,8 +655,8 @@ SmallBwdPlan plan_bwd_small(int ratio, int coff, int head_dim, int capacity, int
     pl.threads_x = groups < kBwdThreads ? groups : kBwdThreads;
     pl.col_slices = (groups + pl.threads_x - 1) / pl.threads_x;
     pl.lanes = kBwdThreads / pl.threads_x > 1 ? kBwdThreads / pl.threads_x : 1;
-    pl.cluster = CSA_BWD_CLUSTER;
-    const int resident = CSA_BWD_MINB * num_sms;  // blocks the register budget is sized for
+    pl.cluster = kBwdCluster;
+    const int resident = kBwdMinBlocks * num_sms;  // blocks the register budget is sized for
     int max_blocks = resident / pl.col_slices;
     max_blocks = max_blocks / pl.cluster * pl.cluster;
     if (max_blocks < pl.cluster)

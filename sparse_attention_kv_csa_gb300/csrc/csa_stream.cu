@@ -1,5 +1,6 @@
 // Streamed Compressor kernels for small ratios: a bulk-copy pipeline into shared
-// memory.  Used when head_dim is a multiple of 128.
+// memory.  Used for ratio 4 when head_dim is a multiple of 64 (the forward from
+// head_dim 128 on).
 //
 // Semantics and operation order are exactly those of csa_small.cu ("CSA Fused
 // Compressor", cuDNN frontend docs, sections Semantics and Numerics): window
@@ -17,8 +18,9 @@
 //     and part for the narrow tiles of a multi-tile head -- and, in the backward,
 //     the grad_out row; completion is counted in bytes on the stage's "full"
 //     mbarrier;
-//   * consumer warps: thread t owns columns [c0 + 2*kNP*t, c0 + 2*kNP*(t + 1)) of
-//     the block's column tile (kNP fp32 pairs, two by default) for every row, so
+//   * consumer warps: thread t owns columns [c0 + 2*NP*t, c0 + 2*NP*(t + 1)) of
+//     the block's column tile (NP fp32 pairs: two where head_dim is a multiple of
+//     128, else one) for every row, so
 //     its APE values stay in registers; it waits on
 //     the stage's "full" barrier, computes from shared memory, writes its outputs
 //     and releases the stage on the "empty" barrier.
@@ -34,52 +36,35 @@
 
 namespace cg = cooperative_groups;
 
-// Ring sizes (bytes of stages per block) and the backward's cluster size.
-#ifndef CSA_STREAM_WHOLE_MAX_D  // widest coff-2 head staged as whole rows
-#define CSA_STREAM_WHOLE_MAX_D 256
-#endif
-#ifndef CSA_STREAM_TMA  // 2-D TMA boxes for tiles of at most 256 columns
-#define CSA_STREAM_TMA 1
-#endif
-#ifndef CSA_STREAM_FWD_BUDGET
-#define CSA_STREAM_FWD_BUDGET (64 * 1024)
-#endif
-#ifndef CSA_STREAM_BWD_BUDGET
-#define CSA_STREAM_BWD_BUDGET (64 * 1024)
-#endif
-#ifndef CSA_STREAM_BWD_CLUSTER
-#define CSA_STREAM_BWD_CLUSTER 2
-#endif
-// Blocks per SM the forward's registers are capped for (1: no cap).
-// Register cap of the forward: at 128 registers five-warp blocks fit three to an
-// SM (each SM sub-partition holds four such warps).
-#ifndef CSA_STREAM_FWD_MAXREG
-#define CSA_STREAM_FWD_MAXREG 128
-#endif
-#ifdef CSA_STREAM_BWD_MAXREG
-#define CSA_STREAM_BWD_BOUNDS __maxnreg__(CSA_STREAM_BWD_MAXREG)
-#else
-#define CSA_STREAM_BWD_BOUNDS __launch_bounds__(kMaxThreads)
-#endif
-
-#ifndef CSA_STREAM_PAIRS
-#define CSA_STREAM_PAIRS 2
-#endif
-
 namespace csa {
 
 namespace {
 
-constexpr int kNP = CSA_STREAM_PAIRS;  // fp32 column pairs per consumer thread
-constexpr int kCPT = 2 * kNP;          // columns per consumer thread
-constexpr int kColsPerWarp = 32 * kCPT;
-static_assert(kNP == 1 || kNP == 2, "CSA_STREAM_PAIRS is 1 or 2");
-constexpr int kMaxThreads = (512 / kColsPerWarp + 1) * 32;  // 512-column tile + the producer warp
+// The plan's fixed choices (each measured on GB300 against its alternatives):
+constexpr int kWholeMaxD = 256;          // widest coff-2 head staged as whole token rows
+constexpr int kFwdBudget = 64 * 1024;    // ring bytes of a forward block with four consumer warps
+constexpr int kBwdBudget = 64 * 1024;    // ... of a backward block
+constexpr int kBwdCluster = 2;           // backward blocks per cluster (grad_ape merged in DSMEM)
+constexpr int kRowLanes1 = 2;            // rows in flight per block when a tile is one warp wide
+// Register cap of the forward: at 128 registers five-warp blocks fit three to an
+// SM (each SM sub-partition holds four such warps).
+constexpr int kFwdMaxReg = 128;
 
-// kNP 32-bit words (2*kNP bf16): one 4- or 8-byte access.
-__device__ __forceinline__ void ld_np(uint32_t (&w)[kNP], const void *p)
+// A consumer thread owns NP fp32 column pairs (NP = 2 where head_dim is a multiple
+// of 128, else 1): CPT columns, and a warp PER_WARP columns of the tile.
+template <int NP>
+struct Cols {
+    static_assert(NP == 1 || NP == 2, "one or two column pairs per thread");
+    static constexpr int CPT = 2 * NP;
+    static constexpr int PER_WARP = 32 * CPT;
+    static constexpr int MAX_THREADS = (512 / PER_WARP + 1) * 32;  // 512-column tile + the producer warp
+};
+
+// NP 32-bit words (2*NP bf16): one 4- or 8-byte access.
+template <int NP>
+__device__ __forceinline__ void ld_np(uint32_t (&w)[NP], const void *p)
 {
-    if constexpr (kNP == 2) {
+    if constexpr (NP == 2) {
         const uint2 v = *reinterpret_cast<const uint2 *>(p);
         w[0] = v.x;
         w[1] = v.y;
@@ -88,26 +73,29 @@ __device__ __forceinline__ void ld_np(uint32_t (&w)[kNP], const void *p)
     }
 }
 
-__device__ __forceinline__ void st_np(void *p, const uint32_t (&w)[kNP])
+template <int NP>
+__device__ __forceinline__ void st_np(void *p, const uint32_t (&w)[NP])
 {
-    if constexpr (kNP == 2)
+    if constexpr (NP == 2)
         *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
     else
         *reinterpret_cast<uint32_t *>(p) = w[0];
 }
 
+template <int NP>
 __device__ __forceinline__ void st_np_zero(void *p)
 {
-    if constexpr (kNP == 2)
+    if constexpr (NP == 2)
         *reinterpret_cast<uint2 *>(p) = make_uint2(0u, 0u);
     else
         *reinterpret_cast<uint32_t *>(p) = 0u;
 }
 
-// kNP fp32 pairs: one 8- or 16-byte access.
-__device__ __forceinline__ void ld_pairs(float2 (&v)[kNP], const float *p)
+// NP fp32 pairs: one 8- or 16-byte access.
+template <int NP>
+__device__ __forceinline__ void ld_pairs(float2 (&v)[NP], const float *p)
 {
-    if constexpr (kNP == 2) {
+    if constexpr (NP == 2) {
         const float4 f = __ldg(reinterpret_cast<const float4 *>(p));
         v[0] = make_float2(f.x, f.y);
         v[1] = make_float2(f.z, f.w);
@@ -116,9 +104,10 @@ __device__ __forceinline__ void ld_pairs(float2 (&v)[kNP], const float *p)
     }
 }
 
-__device__ __forceinline__ void st_pairs(float *p, const float2 (&v)[kNP])
+template <int NP>
+__device__ __forceinline__ void st_pairs(float *p, const float2 (&v)[NP])
 {
-    if constexpr (kNP == 2)
+    if constexpr (NP == 2)
         *reinterpret_cast<float4 *>(p) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
     else
         *reinterpret_cast<float2 *>(p) = v[0];
@@ -137,7 +126,7 @@ struct StreamArgs {
     int stage_bytes;   // bytes per stage (multiple of 128)
     unsigned *status;  // caller-visible status word
     int tc;            // columns of the block's tile
-    int row_lanes;     // rows in flight per block: groups of tc / (32 * 2 * kNP) warps
+    int row_lanes;     // rows in flight per block: groups of tc / (32 * 2 * NP) warps
     int rw;            // elements per staged token row: tc, or C for whole rows
     int pcol;          // whole rows: head_dim (part p's data at column p * head_dim of a row); tiled: 0
     int tma;           // tiled: one 2-D TMA box [RATIO tokens x tc] per array and part
@@ -153,8 +142,8 @@ struct StreamArgs {
 // exchange for 8x fewer, larger copies, which narrow heads need to keep the one
 // issuing thread ahead of the consumers.
 
-// Consumer warp w of a block works on column group w % (tc / kColsPerWarp) of the
-// tile and on row lane w / (tc / kColsPerWarp): the block's j-th row (in the
+// Consumer warp w of a block works on column group w % (tc / PER_WARP) of the
+// tile and on row lane w / (tc / PER_WARP): the block's j-th row (in the
 // producer's order) goes to lane j % row_lanes, in ring slot j % stages.  With
 // stages a multiple of row_lanes every slot always serves the same lane, so no
 // consumer ever waits on a slot more than one phase ahead.
@@ -164,12 +153,13 @@ struct Lanes {
     int lc;    // this thread's first column in the tile
 };
 
+template <int NP>
 __device__ __forceinline__ Lanes lanes_of(const StreamArgs &a, int warp, int lane)
 {
     Lanes l;
-    l.cols = a.tc / kColsPerWarp;
+    l.cols = a.tc / Cols<NP>::PER_WARP;
     l.lane = warp / l.cols;
-    l.lc = ((warp % l.cols) * 32 + lane) * kCPT;
+    l.lc = ((warp % l.cols) * 32 + lane) * Cols<NP>::CPT;
     return l;
 }
 
@@ -301,13 +291,13 @@ __device__ void produce(const StreamArgs &a, const Smem &s, const CUtensorMap *t
 
 // ---------------------------------------------------------------- consumer
 
-template <int RATIO, int COFF>
+template <int RATIO, int COFF, int NP>
 struct ApeRegs {
-    float2 v[COFF * RATIO][kNP];
+    float2 v[COFF * RATIO][NP];
 };
 
-template <int RATIO, int COFF>
-__device__ __forceinline__ void load_ape(const StreamArgs &a, int col0, ApeRegs<RATIO, COFF> &ap)
+template <int RATIO, int COFF, int NP>
+__device__ __forceinline__ void load_ape(const StreamArgs &a, int col0, ApeRegs<RATIO, COFF, NP> &ap)
 {
     const int64_t C = (int64_t)COFF * a.head_dim;
 #pragma unroll
@@ -317,9 +307,9 @@ __device__ __forceinline__ void load_ape(const StreamArgs &a, int col0, ApeRegs<
     }
 }
 
-// Reads the thread's kNP words (2*kNP bf16) of window position k from the stage.
-template <int RATIO, int COFF>
-__device__ __forceinline__ void stage_words(uint32_t (&w)[kNP], const unsigned char *stage, int arr, int k, int rw,
+// Reads the thread's NP words (2*NP bf16) of window position k from the stage.
+template <int RATIO, int COFF, int NP>
+__device__ __forceinline__ void stage_words(uint32_t (&w)[NP], const unsigned char *stage, int arr, int k, int rw,
                                             int pcol, int lc)
 {
     const int p = k / RATIO, i = k % RATIO;
@@ -346,26 +336,26 @@ __device__ __forceinline__ float window_max(const float (&v)[COFF * RATIO], bool
     return first ? a : b;
 }
 
-template <int RATIO, int COFF>
+template <int RATIO, int COFF, int NP>
 __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, int pcol, int lc, bool first,
-                                           const ApeRegs<RATIO, COFF> &ap, uint32_t (&kvw)[COFF * RATIO][kNP],
-                                           float2 (&e)[COFF * RATIO][kNP], float2 (&den)[kNP], float2 (&num)[kNP])
+                                           const ApeRegs<RATIO, COFF, NP> &ap, uint32_t (&kvw)[COFF * RATIO][NP],
+                                           float2 (&e)[COFF * RATIO][NP], float2 (&den)[NP], float2 (&num)[NP])
 {
     constexpr int W = COFF * RATIO;
     // Every position is read; a first block's previous-block positions hold stale
     // stage bytes, which the max below and the sums skip.
 #pragma unroll
     for (int k = 0; k < W; ++k) {
-        uint32_t sw[kNP];
+        uint32_t sw[NP];
         stage_words<RATIO, COFF>(sw, stage, 1, k, rw, pcol, lc);
         stage_words<RATIO, COFF>(kvw[k], stage, 0, k, rw, pcol, lc);
 #pragma unroll
-        for (int q = 0; q < kNP; ++q)
+        for (int q = 0; q < NP; ++q)
             e[k][q] = add2_bf16x2(sw[q], ap.v[k][q]);
     }
-    float2 m[kNP];
+    float2 m[NP];
 #pragma unroll
-    for (int q = 0; q < kNP; ++q) {
+    for (int q = 0; q < NP; ++q) {
         float vx[W], vy[W];
 #pragma unroll
         for (int k = 0; k < W; ++k) {
@@ -374,9 +364,9 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, i
         }
         m[q] = make_float2(window_max<RATIO, COFF>(vx, first), window_max<RATIO, COFF>(vy, first));
     }
-    float2 negm[kNP];
+    float2 negm[NP];
 #pragma unroll
-    for (int q = 0; q < kNP; ++q) {
+    for (int q = 0; q < NP; ++q) {
         negm[q] = make_float2(-m[q].x, -m[q].y);
         den[q] = make_float2(0.0f, 0.0f);
         num[q] = make_float2(0.0f, 0.0f);
@@ -386,7 +376,7 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, i
         if (COFF == 2 && k < RATIO && first)
             continue;
 #pragma unroll
-        for (int q = 0; q < kNP; ++q) {
+        for (int q = 0; q < NP; ++q) {
             const float2 ek = exp2lanes(add2(e[k][q], negm[q]));
             e[k][q] = ek;
             den[q] = add2(den[q], ek);
@@ -397,8 +387,8 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, i
 
 // ----------------------------------------------------------------- forward
 
-template <int RATIO, int COFF>
-__global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG)
+template <int RATIO, int COFF, int NP>
+__global__ void __maxnreg__(kFwdMaxReg)
     fwd_stream_kernel(StreamArgs a, const __grid_constant__ CUtensorMap tm_kv,
                       const __grid_constant__ CUtensorMap tm_sc, uint16_t *__restrict__ out)
 {
@@ -408,7 +398,7 @@ __global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG)
     const int c0 = blockIdx.y * tc;
     const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const Lanes ln = lanes_of(a, warp, lane);
+    const Lanes ln = lanes_of<NP>(a, warp, lane);
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
             mbar_init(smem_addr(&s.full[i]), 1);
@@ -425,8 +415,8 @@ __global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG)
         return;
     }
     const int lc = ln.lc;  // local column of this thread in the tile
-    ApeRegs<RATIO, COFF> ap;
-    load_ape<RATIO, COFF>(a, c0 + lc, ap);
+    ApeRegs<RATIO, COFF, NP> ap;
+    load_ape<RATIO, COFF, NP>(a, c0 + lc, ap);
     int st = ln.lane;
     uint32_t ph = 0;
     for (int j = ln.lane;; j += a.row_lanes, ring_next(st, ph, a.row_lanes, a.stages)) {
@@ -437,15 +427,15 @@ __global__ void __maxnreg__(CSA_STREAM_FWD_MAXREG)
             break;
         const unsigned char *stage = s.stages + (size_t)st * a.stage_bytes;
         const bool first = s.meta[st].first;
-        uint32_t kvw[COFF * RATIO][kNP];
-        float2 e[COFF * RATIO][kNP], den[kNP], num[kNP];
-        pool_stage<RATIO, COFF>(stage, a.rw, a.pcol, lc, first, ap, kvw, e, den, num);
+        uint32_t kvw[COFF * RATIO][NP];
+        float2 e[COFF * RATIO][NP], den[NP], num[NP];
+        pool_stage<RATIO, COFF, NP>(stage, a.rw, a.pcol, lc, first, ap, kvw, e, den, num);
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
-        uint32_t o[kNP];
+        uint32_t o[NP];
 #pragma unroll
-        for (int q = 0; q < kNP; ++q)
+        for (int q = 0; q < NP; ++q)
             o[q] = f2_to_bf16x2(mul2(num[q], make_float2(recip_den(den[q].x), recip_den(den[q].y))));
         st_np(out + (int64_t)row * a.head_dim + c0 + lc, o);
     }
@@ -459,7 +449,7 @@ struct GradOut {
     int64_t n_tokens;
 };
 
-template <int COFF>
+template <int COFF, int NP>
 __device__ __forceinline__ void zero_range(const GradOut &o, int64_t C, int head_dim, int col, int64_t t0,
                                            int64_t t1)
 {
@@ -467,8 +457,8 @@ __device__ __forceinline__ void zero_range(const GradOut &o, int64_t C, int head
     for (int64_t t = t0 < 0 ? 0 : t0; t < t1; ++t) {
 #pragma unroll
         for (int p = 0; p < COFF; ++p) {
-            st_np_zero(o.dkv + t * C + p * head_dim + col);
-            st_np_zero(o.dscore + t * C + p * head_dim + col);
+            st_np_zero<NP>(o.dkv + t * C + p * head_dim + col);
+            st_np_zero<NP>(o.dscore + t * C + p * head_dim + col);
         }
     }
 }
@@ -479,8 +469,8 @@ __device__ __forceinline__ void zero_range(const GradOut &o, int64_t C, int head
 // grad_ape partial of each thread block (its rows in ascending order, per thread)
 // is merged across the cluster in ascending rank order through distributed shared
 // memory; dape_finalize_kernel sums the cluster partials in a fixed order.
-template <int RATIO, int COFF>
-__global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __grid_constant__ CUtensorMap tm_kv,
+template <int RATIO, int COFF, int NP>
+__global__ void __launch_bounds__(Cols<NP>::MAX_THREADS) bwd_stream_kernel(StreamArgs a, const __grid_constant__ CUtensorMap tm_kv,
                                                          const __grid_constant__ CUtensorMap tm_sc, int64_t n_tokens_arg,
                                                          const uint16_t *__restrict__ grad_out,
                                                          uint16_t *__restrict__ dkv, uint16_t *__restrict__ dscore,
@@ -493,7 +483,7 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __gr
     const int c0 = blockIdx.y * tc;
     const Smem s = carve(smem_raw, a.stages, a.stage_bytes);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const Lanes ln = lanes_of(a, warp, lane);
+    const Lanes ln = lanes_of<NP>(a, warp, lane);
     const int64_t C = (int64_t)COFF * a.head_dim;
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
@@ -510,11 +500,11 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __gr
     const int rend = R < a.capacity ? R : a.capacity;  // padding rows carry no gradient
     GradOut o{dkv, dscore, n_tokens_arg >= 0 ? n_tokens_arg : (int64_t)__ldg(a.cu + a.n_seg)};
 
-    float2 acc[W][kNP];
+    float2 acc[W][NP];
 #pragma unroll
     for (int k = 0; k < W; ++k)
 #pragma unroll
-        for (int q = 0; q < kNP; ++q)
+        for (int q = 0; q < NP; ++q)
             acc[k][q] = make_float2(0.0f, 0.0f);
     const int lc = ln.lc;
     const int col = c0 + lc;
@@ -527,10 +517,10 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __gr
             int64_t lead = o.n_tokens;
             if (R0 < R)
                 lead = map_row(R0, a.cu, a.cc, a.n_seg, RATIO).base;
-            zero_range<COFF>(o, C, a.head_dim, col, 0, lead);
+            zero_range<COFF, NP>(o, C, a.head_dim, col, 0, lead);
         }
-        ApeRegs<RATIO, COFF> ap;
-        load_ape<RATIO, COFF>(a, col, ap);
+        ApeRegs<RATIO, COFF, NP> ap;
+        load_ape<RATIO, COFF, NP>(a, col, ap);
         int st_used = ln.lane;
         uint32_t ph = 0;
         for (int j = ln.lane;; j += a.row_lanes, ring_next(st_used, ph, a.row_lanes, a.stages)) {
@@ -546,17 +536,17 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __gr
                 continue;
             }
             const unsigned char *stage = s.stages + (size_t)st_used * a.stage_bytes;
-            uint32_t kvw[W][kNP];
-            float2 e[W][kNP], den[kNP], num[kNP];
-            pool_stage<RATIO, COFF>(stage, a.rw, a.pcol, lc, m.first, ap, kvw, e, den, num);
-            uint32_t gw[kNP];
+            uint32_t kvw[W][NP];
+            float2 e[W][NP], den[NP], num[NP];
+            pool_stage<RATIO, COFF, NP>(stage, a.rw, a.pcol, lc, m.first, ap, kvw, e, den, num);
+            uint32_t gw[NP];
             ld_np(gw, stage + window_bytes<RATIO, COFF>(a.rw) + lc * 2);
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&s.empty[st_used]));
-            float2 g[kNP], inv[kNP], ngo[kNP];
+            float2 g[NP], inv[NP], ngo[NP];
 #pragma unroll
-            for (int q = 0; q < kNP; ++q) {
+            for (int q = 0; q < NP; ++q) {
                 g[q] = bf16x2_to_f2(gw[q]);
                 inv[q] = make_float2(recip_den(den[q].x), recip_den(den[q].y));
                 const float2 go = mul2(g[q], mul2(num[q], inv[q]));
@@ -568,9 +558,9 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __gr
                     continue;
                 const int p = k / RATIO, i = k % RATIO;
                 const int64_t tok = m.base + (int64_t)(p - (COFF - 1)) * RATIO + i;
-                uint32_t dk[kNP], dsw[kNP];
+                uint32_t dk[NP], dsw[NP];
 #pragma unroll
-                for (int q = 0; q < kNP; ++q) {
+                for (int q = 0; q < NP; ++q) {
                     const float2 pk = mul2(e[k][q], inv[q]);
                     dk[q] = f2_to_bf16x2(mul2(g[q], pk));
                     const float2 ds = mul2(pk, add2(mul2(g[q], bf16x2_to_f2(kvw[k][q])), ngo[q]));
@@ -588,15 +578,15 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __gr
                     for (int i = 0; i < RATIO; ++i) {
                         const int64_t tok = m.base + i;
                         if (tok < o.n_tokens) {
-                            st_np_zero(dkv + tok * C + col);
-                            st_np_zero(dscore + tok * C + col);
+                            st_np_zero<NP>(dkv + tok * C + col);
+                            st_np_zero<NP>(dscore + tok * C + col);
                         }
                     }
                 }
                 int64_t next = o.n_tokens;
                 if (m.row + 1 < R)
                     next = map_row(m.row + 1, a.cu, a.cc, a.n_seg, RATIO).base;
-                zero_range<COFF>(o, C, a.head_dim, col, m.base + RATIO, next);
+                zero_range<COFF, NP>(o, C, a.head_dim, col, m.base + RATIO, next);
             }
         }
         // this thread's grad_ape sums -> shared memory [row lane][ape row][part][tile column]
@@ -638,31 +628,38 @@ __global__ void CSA_STREAM_BWD_BOUNDS bwd_stream_kernel(StreamArgs a, const __gr
     cluster.sync();
 }
 
-// Widest tile of at most 512 columns (whole consumer warps) that divides head_dim.
-int tile_cols(int head_dim)
+// Widest tile of at most 512 columns (whole consumer warps of cpw columns) that
+// divides head_dim.
+int tile_cols(int head_dim, int cpw)
 {
-    for (int w = 512 / kColsPerWarp; w >= 1; --w)
-        if (head_dim % (w * kColsPerWarp) == 0)
-            return w * kColsPerWarp;
+    for (int w = 512 / cpw; w >= 1; --w)
+        if (head_dim % (w * cpw) == 0)
+            return w * cpw;
     return 0;
 }
 
 }  // namespace
 
-bool stream_supported(int ratio, int coff, int head_dim)
+bool stream_supported(bool bwd, int ratio, int coff, int head_dim)
 {
-    return ratio == 4 && (coff == 1 || coff == 2) && head_dim % 128 == 0;
+    if (ratio != 4 || (coff != 1 && coff != 2) || head_dim % 64 != 0 || head_dim > 8192)
+        return false;
+    // head_dim 64, forward: the register-window kernel measured faster (21.3 against
+    // 32.9 us at 32 x 4096 tokens, coff 2; the backward 69.0 against 51.8 us)
+    return bwd || head_dim > 64;
 }
 
 StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity, int num_sms)
 {
     StreamPlan pl;
-    pl.tc = tile_cols(head_dim);
+    pl.np = head_dim % 128 == 0 ? 2 : 1;
+    const int cpw = 64 * pl.np;  // columns per consumer warp
+    pl.tc = tile_cols(head_dim, cpw);
     pl.tiles = head_dim / pl.tc;
-    // Up to four consumer warps per block: tiles narrower than 512 columns take
-    // two rows at once (more would leave the block's one producer behind).
-    const int cols = pl.tc / kColsPerWarp;
-    pl.row_lanes = cols <= 2 ? 2 : 1;
+    // Up to four consumer warps per block: tiles of one or two warps take several
+    // rows at once (more would leave the block's one producer behind).
+    const int cols = pl.tc / cpw;
+    pl.row_lanes = cols == 1 ? kRowLanes1 : cols == 2 ? 2 : 1;
     const int warps = cols * pl.row_lanes;
     pl.threads = (warps + 1) * 32;
     // One column tile: whole token rows when the head is narrow enough (coff 2
@@ -671,29 +668,31 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     // and part (head_dim 640, coff 1: forward 34.0 -> 28.7 us against one bulk copy
     // per token; a single coff-2 tile of 128 or 256 columns measured no faster
     // with boxes than with whole rows).
-    pl.whole = pl.tiles == 1 && (coff == 1 || head_dim <= CSA_STREAM_WHOLE_MAX_D);
-    pl.tma = CSA_STREAM_TMA && !pl.whole && pl.tc <= 256;
+    pl.whole = pl.tiles == 1 && (coff == 1 || head_dim <= kWholeMaxD);
+    pl.tma = !pl.whole && pl.tc <= 256;
     const int rw = pl.whole ? coff * head_dim : pl.tc;
     const int win = 2 * coff * ratio * rw * 2;
     pl.stage_bytes = ((bwd ? win + pl.tc * 2 : win) + 127) / 128 * 128;
     // ring bytes in proportion to the consumer warps (the budget is for four)
-    const int budget = (bwd ? CSA_STREAM_BWD_BUDGET : CSA_STREAM_FWD_BUDGET) / 4 * warps;
+    const int budget = (bwd ? kBwdBudget : kFwdBudget) / 4 * warps;
     int per_lane = budget / pl.stage_bytes / pl.row_lanes;
     per_lane = per_lane < 2 ? 2 : (per_lane > 8 ? 8 : per_lane);
     pl.stages = per_lane * pl.row_lanes;  // a multiple of the row lanes
     pl.red_bytes = bwd ? (size_t)pl.row_lanes * ratio * coff * pl.tc * sizeof(float) : 0;
     pl.smem = smem_bytes(pl.stages, pl.stage_bytes, pl.red_bytes);
-    pl.cluster = bwd ? CSA_STREAM_BWD_CLUSTER : 1;
+    pl.cluster = bwd ? kBwdCluster : 1;
     pl.num_sms = num_sms;
     (void)capacity;
     return pl;
 }
 
-template <int RATIO, int COFF>
-static cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out)
+namespace {
+
+template <int RATIO, int COFF, int NP>
+cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out)
 {
-    const void *fn = bwd ? reinterpret_cast<const void *>(bwd_stream_kernel<RATIO, COFF>)
-                         : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF>);
+    const void *fn = bwd ? reinterpret_cast<const void *>(bwd_stream_kernel<RATIO, COFF, NP>)
+                         : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF, NP>);
     int resident = 0;
     cudaError_t e = resident_blocks(fn, pl.threads, pl.smem, pl.cluster, &resident);
     if (e != cudaSuccess)
@@ -709,24 +708,37 @@ static cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out
     return cudaSuccess;
 }
 
-template <int RATIO, int COFF>
-static cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl, unsigned *status,
-                                       cudaStream_t st)
+StreamArgs stream_args(const void *kv, const void *score, const float *ape, const int32_t *cu, const int32_t *cc,
+                       int n_seg, int coff, int head_dim, int capacity, const StreamPlan &pl, unsigned *status)
 {
-    StreamArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
-                 p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes,
-                 status, pl.tc, pl.row_lanes, pl.whole ? p.coff * p.head_dim : pl.tc, pl.whole ? p.head_dim : 0,
-                 pl.tma ? 1 : 0};
+    return StreamArgs{static_cast<const uint16_t *>(kv), static_cast<const uint16_t *>(score), ape, cu, cc, n_seg,
+                      head_dim, capacity, pl.stages, pl.stage_bytes, status, pl.tc, pl.row_lanes,
+                      pl.whole ? coff * head_dim : pl.tc, pl.whole ? head_dim : 0, pl.tma ? 1 : 0};
+}
+
+template <int RATIO>
+cudaError_t stream_maps(const StreamPlan &pl, const void *kv, const void *score, int64_t C, CUtensorMap *mk,
+                        CUtensorMap *ms)
+{
+    if (!pl.tma)
+        return cudaSuccess;
+    cudaError_t e = make_tensor_map_2d(mk, kv, C, pl.tc, RATIO);
+    if (e == cudaSuccess)
+        e = make_tensor_map_2d(ms, score, C, pl.tc, RATIO);
+    return e;
+}
+
+template <int RATIO, int COFF, int NP>
+cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st)
+{
+    const StreamArgs a = stream_args(p.kv, p.score, p.ape, p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.coff,
+                                     p.head_dim, p.capacity, pl, status);
     CUtensorMap mk{}, ms{};
-    if (pl.tma) {
-        cudaError_t me = make_tensor_map_2d(&mk, p.kv, (int64_t)p.coff * p.head_dim, pl.tc, RATIO);
-        if (me == cudaSuccess)
-            me = make_tensor_map_2d(&ms, p.score, (int64_t)p.coff * p.head_dim, pl.tc, RATIO);
-        if (me != cudaSuccess)
-            return me;
-    }
+    cudaError_t e = stream_maps<RATIO>(pl, p.kv, p.score, (int64_t)p.coff * p.head_dim, &mk, &ms);
+    if (e != cudaSuccess)
+        return e;
     int blocks = 0;
-    cudaError_t e = blocks_for<RATIO, COFF>(pl, false, p.capacity, &blocks);
+    e = blocks_for<RATIO, COFF, NP>(pl, false, p.capacity, &blocks);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -737,52 +749,37 @@ static cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl,
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<RATIO, COFF>, a, mk, ms, static_cast<uint16_t *>(p.out));
+    return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<RATIO, COFF, NP>, a, mk, ms, static_cast<uint16_t *>(p.out));
 }
 
-cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st)
+// The exact grid width of the backward: the resident blocks, at most the upper
+// bound stream_bwd_partials sizes the workspace for.
+template <int RATIO, int COFF, int NP>
+cudaError_t stream_bwd_blocks_t(const StreamPlan &pl, int capacity, int *out)
 {
-    if (p.ratio == 4 && p.coff == 2)
-        return launch_fwd_stream_t<4, 2>(p, pl, status, st);
-    if (p.ratio == 4 && p.coff == 1)
-        return launch_fwd_stream_t<4, 1>(p, pl, status, st);
-    return cudaErrorInvalidValue;
-}
-
-// Upper bound of grad_ape partials (cluster count) for the workspace size.
-int stream_bwd_partials(const StreamPlan &pl, int capacity)
-{
-    const int rows = capacity > 0 ? capacity : 1;
-    int blocks = 8 * pl.num_sms / pl.tiles;  // never more than 8 resident per SM
-    if (blocks > rows)
-        blocks = rows;
-    blocks = (blocks + pl.cluster - 1) / pl.cluster * pl.cluster;
-    return blocks / pl.cluster;
-}
-
-template <int RATIO, int COFF>
-static cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
-                                       cudaStream_t st)
-{
-    StreamArgs a{static_cast<const uint16_t *>(p.kv), static_cast<const uint16_t *>(p.score), p.ape,
-                 p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.head_dim, p.capacity, pl.stages, pl.stage_bytes,
-                 status, pl.tc, pl.row_lanes, pl.whole ? p.coff * p.head_dim : pl.tc, pl.whole ? p.head_dim : 0,
-                 pl.tma ? 1 : 0};
-    CUtensorMap mk{}, ms{};
-    if (pl.tma) {
-        cudaError_t me = make_tensor_map_2d(&mk, p.kv, (int64_t)p.coff * p.head_dim, pl.tc, RATIO);
-        if (me == cudaSuccess)
-            me = make_tensor_map_2d(&ms, p.score, (int64_t)p.coff * p.head_dim, pl.tc, RATIO);
-        if (me != cudaSuccess)
-            return me;
-    }
     int blocks = 0;
-    cudaError_t e = blocks_for<RATIO, COFF>(pl, true, p.capacity, &blocks);
+    cudaError_t e = blocks_for<RATIO, COFF, NP>(pl, true, capacity, &blocks);
     if (e != cudaSuccess)
         return e;
-    const int max_blocks = stream_bwd_partials(pl, p.capacity) * pl.cluster;
-    if (blocks > max_blocks)
-        blocks = max_blocks;
+    const int max_blocks = stream_bwd_partials(pl, capacity) * pl.cluster;
+    *out = blocks > max_blocks ? max_blocks : blocks;
+    return cudaSuccess;
+}
+
+template <int RATIO, int COFF, int NP>
+cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
+                                cudaStream_t st)
+{
+    const StreamArgs a = stream_args(p.kv, p.score, p.ape, p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.coff,
+                                     p.head_dim, p.capacity, pl, status);
+    CUtensorMap mk{}, ms{};
+    cudaError_t e = stream_maps<RATIO>(pl, p.kv, p.score, (int64_t)p.coff * p.head_dim, &mk, &ms);
+    if (e != cudaSuccess)
+        return e;
+    int blocks = 0;
+    e = stream_bwd_blocks_t<RATIO, COFF, NP>(pl, p.capacity, &blocks);
+    if (e != cudaSuccess)
+        return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks, pl.tiles, 1);
     cfg.blockDim = dim3(pl.threads, 1, 1);
@@ -796,7 +793,7 @@ static cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl,
     attr[1] = pdl_attribute();
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, bwd_stream_kernel<RATIO, COFF>, a, mk, ms, p.n_tokens,
+    e = cudaLaunchKernelEx(&cfg, bwd_stream_kernel<RATIO, COFF, NP>, a, mk, ms, p.n_tokens,
                            static_cast<const uint16_t *>(p.grad_out), static_cast<uint16_t *>(p.dkv),
                            static_cast<uint16_t *>(p.dscore), partial);
     if (e != cudaSuccess)
@@ -804,35 +801,48 @@ static cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl,
     return launch_dape_finalize(partial, blocks / pl.cluster, (int64_t)RATIO * COFF * p.head_dim, p.dape, st);
 }
 
-template <int RATIO, int COFF>
-static cudaError_t stream_bwd_blocks_t(const StreamPlan &pl, int capacity, int *out)
+}  // namespace
+
+// The kernel instance of a plan: ratio 4, the window form, the column pairs per
+// thread.
+#define CSA_STREAM_DISPATCH(FN, ...)                                                        \
+    do {                                                                                    \
+        if (ratio != 4 || (coff != 1 && coff != 2) || (pl.np != 1 && pl.np != 2))           \
+            return cudaErrorInvalidValue;                                                   \
+        if (coff == 2)                                                                      \
+            return pl.np == 2 ? FN<4, 2, 2>(__VA_ARGS__) : FN<4, 2, 1>(__VA_ARGS__);        \
+        return pl.np == 2 ? FN<4, 1, 2>(__VA_ARGS__) : FN<4, 1, 1>(__VA_ARGS__);            \
+    } while (0)
+
+cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st)
 {
-    int blocks = 0;
-    cudaError_t e = blocks_for<RATIO, COFF>(pl, true, capacity, &blocks);
-    if (e != cudaSuccess)
-        return e;
-    const int max_blocks = stream_bwd_partials(pl, capacity) * pl.cluster;
-    *out = blocks > max_blocks ? max_blocks : blocks;
-    return cudaSuccess;
+    const int ratio = p.ratio, coff = p.coff;
+    CSA_STREAM_DISPATCH(launch_fwd_stream_t, p, pl, status, st);
+}
+
+// Upper bound of grad_ape partials (cluster count) for the workspace size.
+int stream_bwd_partials(const StreamPlan &pl, int capacity)
+{
+    const int rows = capacity > 0 ? capacity : 1;
+    int blocks = 8 * pl.num_sms / pl.tiles;  // never more than 8 resident per SM
+    if (blocks > rows)
+        blocks = rows;
+    blocks = (blocks + pl.cluster - 1) / pl.cluster * pl.cluster;
+    return blocks / pl.cluster;
 }
 
 cudaError_t stream_bwd_blocks(int ratio, int coff, const StreamPlan &pl, int capacity, int *blocks)
 {
-    if (ratio == 4 && coff == 2)
-        return stream_bwd_blocks_t<4, 2>(pl, capacity, blocks);
-    if (ratio == 4 && coff == 1)
-        return stream_bwd_blocks_t<4, 1>(pl, capacity, blocks);
-    return cudaErrorInvalidValue;
+    CSA_STREAM_DISPATCH(stream_bwd_blocks_t, pl, capacity, blocks);
 }
 
 cudaError_t launch_bwd_stream(const BwdParams &p, const StreamPlan &pl, float *partial, unsigned *status,
                               cudaStream_t st)
 {
-    if (p.ratio == 4 && p.coff == 2)
-        return launch_bwd_stream_t<4, 2>(p, pl, partial, status, st);
-    if (p.ratio == 4 && p.coff == 1)
-        return launch_bwd_stream_t<4, 1>(p, pl, partial, status, st);
-    return cudaErrorInvalidValue;
+    const int ratio = p.ratio, coff = p.coff;
+    CSA_STREAM_DISPATCH(launch_bwd_stream_t, p, pl, partial, status, st);
 }
+
+#undef CSA_STREAM_DISPATCH
 
 }  // namespace csa

@@ -250,9 +250,10 @@ def test_misaligned_view_is_rejected_and_nothing_written(csa):
 
 
 def test_both_kernel_families_agree_bitwise(csa):
-    """head_dim 384 (a multiple of 128: the bulk-copy pipeline) and 392 (not: the
-    register kernels) on the same rows give the oracle's bits in both."""
-    for D in (384, 392):
+    """head_dim 384 (a multiple of 128: the bulk-copy pipeline, two column pairs per
+    thread), 320 (a multiple of 64: the pipeline, one pair) and 392 (neither: the
+    register kernels) on the same rows give the oracle's bits in all three."""
+    for D in (384, 320, 392):
         c = w.make_case("fam", 4, 2, D, [57, 4, 130], extra_rows=2, seed=12)
         d = Dev(c)
         assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))

@@ -40,7 +40,7 @@ def run_noalloc(d, csa, canary, n_tokens=None, capacity=None):
     return dkv.cpu().numpy().view(np.uint16), dsc.cpu().numpy().view(np.uint16), dape.cpu().numpy()
 
 
-@pytest.mark.parametrize("head_dim", [512, 64])  # bulk-copy pipeline / register kernels
+@pytest.mark.parametrize("head_dim", [512, 64, 96])  # bulk-copy pipeline (two / one pairs) / register kernels
 def test_noalloc_matches_backward_two_calls_in_a_row(csa, head_dim):
     cases = [w.make_case("na%d" % s, 4, 2, head_dim, [4096, 37, 2, 1100], extra_rows=16, seed=s)
              for s in (31, 32)]
