@@ -21,7 +21,9 @@
 // order, checked against the plain sequential oracle by tolerance; the library
 // applies the same contract to every window of more than 64 positions):
 //   s_k = score + ape;  m = max over all valid k (exact: chunk maxima, then over
-//   the warp's chunks by shuffles, then over the consumer warps);
+//   the warp's chunks by shuffles, then over the consumer warps; with coff 1 each
+//   warp first uses its own maximum m_w and the merge below rescales its sums by
+//   2^((m_w - m) log2 e));
 //   e_k = 2^(s_k*log2(e) - m*log2(e)) on the multi-function unit (ex2.approx, as
 //   the page's ratio-128 kernels do: ~2^-22 relative error, far below the final
 //   bf16 rounding);
@@ -78,6 +80,12 @@ struct Geo {
     // blocks (ratio 64 with coff 2: forward 32.1 -> 29.7 us, backward 66.5 -> 64.8
     // us at 8 x 4096 tokens, head_dim 512), else two
     static constexpr int MIN_BLOCKS = CW == 4 ? 3 : 2;
+    // coff 1: each warp's terms are taken relative to the warp's own maximum and
+    // the merge rescales them to the row's (one block barrier fewer per row;
+    // ratio 128 backward 100.6 -> 97.4 us, ratio 96 forward / backward 26.4 / 63.2
+    // -> 24.4 / 60.5 us); coff 2 keeps the row maximum first (faster there:
+    // ratio-128 backward 222 against 230 us)
+    static constexpr bool LOCAL = COFF == 1;
     static_assert(CW * CPW == NC, "chunks per warp");
 };
 
@@ -154,7 +162,7 @@ struct ChSmem {
     float *mx;   // [2][CW][RS]  warp maxima
     float *den;  // [2][CW][RS]  warp sums
     float *num;  // [2][CW][RS]
-    float *fin;  // [2][2][TC]  (inv, o) for the backward
+    float *fin;  // [2][2 + CW][TC]  (inv, o, each warp's scale) for the backward
     float *apet; // [WMAX][TC]  the backward's APE tile (null in the forward)
     Meta *meta;
     uint64_t *full;
@@ -165,7 +173,7 @@ template <int COFF, int NCB>
 __host__ __device__ size_t ch_smem_bytes(int stages, int stage_bytes, bool ape_tile)
 {
     using G = Geo<COFF, NCB>;
-    return (size_t)stages * stage_bytes + 3 * 2 * G::CW * G::RS * 4 + 2 * 2 * G::TC * 4 +
+    return (size_t)stages * stage_bytes + 3 * 2 * G::CW * G::RS * 4 + 2 * (2 + G::CW) * G::TC * 4 +
            (ape_tile ? (size_t)G::WMAX * G::TC * 4 : 0) + sizeof(Meta) * stages + 16 * stages + 16;
 }
 
@@ -180,8 +188,8 @@ __device__ __forceinline__ ChSmem<COFF, NCB> ch_carve(unsigned char *base, int s
     s.den = s.mx + 2 * G::CW * G::RS;
     s.num = s.den + 2 * G::CW * G::RS;
     s.fin = s.num + 2 * G::CW * G::RS;
-    s.apet = ape_tile ? s.fin + 2 * 2 * G::TC : nullptr;
-    p = reinterpret_cast<unsigned char *>(s.fin + 2 * 2 * G::TC + (ape_tile ? G::WMAX * G::TC : 0));
+    s.apet = ape_tile ? s.fin + 2 * (2 + G::CW) * G::TC : nullptr;
+    p = reinterpret_cast<unsigned char *>(s.fin + 2 * (2 + G::CW) * G::TC + (ape_tile ? G::WMAX * G::TC : 0));
     s.meta = reinterpret_cast<Meta *>(p);
     s.full = reinterpret_cast<uint64_t *>(s.meta + stages);
     s.empty = s.full + stages;
@@ -363,18 +371,26 @@ __device__ __forceinline__ bool ch_pool(const Win<COFF, NCB, RC> &w, const ChSme
         for (int q = 0; q < 4; ++q)
             m[q] = max_nan(m[q], __shfl_xor_sync(0xffffffffu, m[q], d));
     float *mx = s.mx + (size_t)buf * G::CW * G::RS;
-    if (lane < G::G)
-        *reinterpret_cast<float4 *>(mx + warp * G::RS + 4 * g) = make_float4(m[0], m[1], m[2], m[3]);
-    if (!named_barrier_and(1, G::CT, ok))
-        return false;
-    float4 M = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    float4 M;
+    if constexpr (G::LOCAL) {
+        // the warp's maximum is its terms' reference (0 where it is -inf: those
+        // terms all vanish); ch_final rescales the warp sums to the row's maximum
+        M = make_float4(m[0] == -INFINITY ? 0.0f : m[0], m[1] == -INFINITY ? 0.0f : m[1],
+                        m[2] == -INFINITY ? 0.0f : m[2], m[3] == -INFINITY ? 0.0f : m[3]);
+    } else {
+        if (lane < G::G)
+            *reinterpret_cast<float4 *>(mx + warp * G::RS + 4 * g) = make_float4(m[0], m[1], m[2], m[3]);
+        if (!named_barrier_and(1, G::CT, ok))
+            return false;
+        M = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
 #pragma unroll
-    for (int v = 0; v < G::CW; ++v) {
-        const float4 x = *reinterpret_cast<const float4 *>(mx + v * G::RS + 4 * g);
-        M.x = max_nan(M.x, x.x);
-        M.y = max_nan(M.y, x.y);
-        M.z = max_nan(M.z, x.z);
-        M.w = max_nan(M.w, x.w);
+        for (int v = 0; v < G::CW; ++v) {
+            const float4 x = *reinterpret_cast<const float4 *>(mx + v * G::RS + 4 * g);
+            M.x = max_nan(M.x, x.x);
+            M.y = max_nan(M.y, x.y);
+            M.z = max_nan(M.z, x.z);
+            M.w = max_nan(M.w, x.w);
+        }
     }
     float2 den[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
     float2 num[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
@@ -410,9 +426,13 @@ __device__ __forceinline__ bool ch_pool(const Win<COFF, NCB, RC> &w, const ChSme
     if (lane < G::G) {
         float *dn = s.den + (size_t)buf * G::CW * G::RS;
         float *nm = s.num + (size_t)buf * G::CW * G::RS;
+        if constexpr (G::LOCAL)
+            *reinterpret_cast<float4 *>(mx + warp * G::RS + 4 * g) = make_float4(m[0], m[1], m[2], m[3]);
         *reinterpret_cast<float4 *>(dn + warp * G::RS + 4 * g) = make_float4(den[0].x, den[0].y, den[1].x, den[1].y);
         *reinterpret_cast<float4 *>(nm + warp * G::RS + 4 * g) = make_float4(num[0].x, num[0].y, num[1].x, num[1].y);
     }
+    if constexpr (G::LOCAL)
+        return named_barrier_and(1, G::CT, ok);
     named_barrier(1, G::CT);
     return true;
 }
@@ -422,7 +442,8 @@ __device__ __forceinline__ bool ch_pool(const Win<COFF, NCB, RC> &w, const ChSme
 // order, then the TPC partial sums meet in a fixed xor-shuffle tree, so every one
 // of them ends with the same den and num of column j.
 template <int COFF, int NCB>
-__device__ __forceinline__ void ch_final(const ChSmem<COFF, NCB> &s, int buf, int &j, float &den, float &num)
+__device__ __forceinline__ void ch_final(const ChSmem<COFF, NCB> &s, int buf, int &j, float &den, float &num,
+                                         float *scale)
 {
     using G = Geo<COFF, NCB>;
     constexpr int TPC = G::CT / G::TC;  // threads per column
@@ -432,12 +453,38 @@ __device__ __forceinline__ void ch_final(const ChSmem<COFF, NCB> &s, int buf, in
     const int q = (int)threadIdx.x % TPC;
     const float *dn = s.den + (size_t)buf * G::CW * G::RS + q * WPT * G::RS + j;
     const float *nm = s.num + (size_t)buf * G::CW * G::RS + q * WPT * G::RS + j;
-    den = dn[0];
-    num = nm[0];
+    if constexpr (G::LOCAL) {
+        // the row's maximum over the warps' maxima; each warp's sums rescaled by
+        // 2^((m_w - M) log2 e) (0 for a warp whose terms all vanished), added in
+        // ascending warp order, then the fixed xor tree
+        const float *mx = s.mx + (size_t)buf * G::CW * G::RS + q * WPT * G::RS + j;
+        float M = mx[0];
 #pragma unroll
-    for (int v = 1; v < WPT; ++v) {
-        den = __fadd_rn(den, dn[v * G::RS]);
-        num = __fadd_rn(num, nm[v * G::RS]);
+        for (int v = 1; v < WPT; ++v)
+            M = max_nan(M, mx[v * G::RS]);
+#pragma unroll
+        for (int d = 1; d < TPC; d *= 2)
+            M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, d));
+        const float nml = -__fmul_rn(M, kLog2eF);
+        den = 0.0f;
+        num = 0.0f;
+#pragma unroll
+        for (int v = 0; v < WPT; ++v) {
+            const float mw = mx[v * G::RS];
+            const float sc = mw == -INFINITY ? 0.0f : ex2_fast(__fmaf_rn(mw, kLog2eF, nml));
+            den = __fmaf_rn(dn[v * G::RS], sc, den);
+            num = __fmaf_rn(nm[v * G::RS], sc, num);
+            if (scale)
+                scale[(q * WPT + v) * G::TC + j] = sc;
+        }
+    } else {
+        den = dn[0];
+        num = nm[0];
+#pragma unroll
+        for (int v = 1; v < WPT; ++v) {
+            den = __fadd_rn(den, dn[v * G::RS]);
+            num = __fadd_rn(num, nm[v * G::RS]);
+        }
     }
 #pragma unroll
     for (int d = 1; d < TPC; d *= 2) {
@@ -520,7 +567,7 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, Geo<COFF, NCB>::MIN_B
         {
             int j;
             float den, num;
-            ch_final<COFF, NCB>(s, buf, j, den, num);
+            ch_final<COFF, NCB>(s, buf, j, den, num, nullptr);
             if (threadIdx.x % (G::CT / G::TC) == 0) {
                 const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, recip_den(den)));
                 out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
@@ -639,11 +686,11 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF> ? Geo<
                 break;
             const float2 gg[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
             const uint32_t gwq[2] = {gw.x, gw.y};
-            float *fin = s.fin + (size_t)buf * 2 * G::TC;
+            float *fin = s.fin + (size_t)buf * (2 + G::CW) * G::TC;
             {
                 int j;
                 float den, num;
-                ch_final<COFF, NCB>(s, buf, j, den, num);
+                ch_final<COFF, NCB>(s, buf, j, den, num, G::LOCAL ? fin + 2 * G::TC : nullptr);
                 if (threadIdx.x % (G::CT / G::TC) == 0 && m.real) {
                     const float inv = recip_den(den);
                     fin[j] = inv;
@@ -662,7 +709,12 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF> ? Geo<
             }
             const float4 inv4 = *reinterpret_cast<const float4 *>(fin + 4 * g);
             const float4 o4 = *reinterpret_cast<const float4 *>(fin + G::TC + 4 * g);
-            const float2 inv[2] = {make_float2(inv4.x, inv4.y), make_float2(inv4.z, inv4.w)};
+            float2 inv[2] = {make_float2(inv4.x, inv4.y), make_float2(inv4.z, inv4.w)};
+            if constexpr (G::LOCAL) {  // p_k = e_k * scale_w * inv: e_k is relative to the warp's maximum
+                const float4 sc4 = *reinterpret_cast<const float4 *>(fin + (2 + warp) * G::TC + 4 * g);
+                inv[0] = mul2(inv[0], make_float2(sc4.x, sc4.y));
+                inv[1] = mul2(inv[1], make_float2(sc4.z, sc4.w));
+            }
             const float2 go[2] = {mul2(gg[0], make_float2(o4.x, o4.y)), mul2(gg[1], make_float2(o4.z, o4.w))};
             const float2 ngo[2] = {make_float2(-go[0].x, -go[0].y), make_float2(-go[1].x, -go[1].y)};
             // window position k = c + NC*i sits at token t0 + k (part = k / ratio)

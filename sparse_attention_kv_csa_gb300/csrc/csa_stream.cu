@@ -336,23 +336,31 @@ __device__ __forceinline__ float window_max(const float (&v)[COFF * RATIO], bool
     return first ? a : b;
 }
 
+// Reads a row's window words (score and kv, the thread's columns) from its stage.
 template <int RATIO, int COFF, int NP>
-__device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, int pcol, int lc, bool first,
-                                           const ApeRegs<RATIO, COFF, NP> &ap, uint32_t (&kvw)[COFF * RATIO][NP],
-                                           float2 (&e)[COFF * RATIO][NP], float2 (&den)[NP], float2 (&num)[NP])
+__device__ __forceinline__ void stage_load(const unsigned char *stage, int rw, int pcol, int lc,
+                                           uint32_t (&sw)[COFF * RATIO][NP], uint32_t (&kvw)[COFF * RATIO][NP])
+{
+#pragma unroll
+    for (int k = 0; k < COFF * RATIO; ++k) {
+        stage_words<RATIO, COFF>(sw[k], stage, 1, k, rw, pcol, lc);
+        stage_words<RATIO, COFF>(kvw[k], stage, 0, k, rw, pcol, lc);
+    }
+}
+
+// The pooling of one row from its words in registers (a first block's
+// previous-block positions hold stale words, which the max and the sums skip).
+template <int RATIO, int COFF, int NP>
+__device__ __forceinline__ void pool_regs(const uint32_t (&sw)[COFF * RATIO][NP], const uint32_t (&kvw)[COFF * RATIO][NP],
+                                          bool first, const ApeRegs<RATIO, COFF, NP> &ap,
+                                          float2 (&e)[COFF * RATIO][NP], float2 (&den)[NP], float2 (&num)[NP])
 {
     constexpr int W = COFF * RATIO;
-    // Every position is read; a first block's previous-block positions hold stale
-    // stage bytes, which the max below and the sums skip.
 #pragma unroll
-    for (int k = 0; k < W; ++k) {
-        uint32_t sw[NP];
-        stage_words<RATIO, COFF>(sw, stage, 1, k, rw, pcol, lc);
-        stage_words<RATIO, COFF>(kvw[k], stage, 0, k, rw, pcol, lc);
+    for (int k = 0; k < W; ++k)
 #pragma unroll
         for (int q = 0; q < NP; ++q)
-            e[k][q] = add2_bf16x2(sw[q], ap.v[k][q]);
-    }
+            e[k][q] = add2_bf16x2(sw[k][q], ap.v[k][q]);
     float2 m[NP];
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
@@ -383,6 +391,16 @@ __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, i
             num[q] = fma2(ek, bf16x2_to_f2(kvw[k][q]), num[q]);
         }
     }
+}
+
+template <int RATIO, int COFF, int NP>
+__device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, int pcol, int lc, bool first,
+                                           const ApeRegs<RATIO, COFF, NP> &ap, uint32_t (&kvw)[COFF * RATIO][NP],
+                                           float2 (&e)[COFF * RATIO][NP], float2 (&den)[NP], float2 (&num)[NP])
+{
+    uint32_t sw[COFF * RATIO][NP];
+    stage_load<RATIO, COFF, NP>(stage, rw, pcol, lc, sw, kvw);
+    pool_regs<RATIO, COFF, NP>(sw, kvw, first, ap, e, den, num);
 }
 
 // ----------------------------------------------------------------- forward
