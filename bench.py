@@ -5,7 +5,10 @@ capacity 8256; seeded synthetic inputs from csa_workloads).
 
 Prints one JSON line.  `value` is input tokens per second of the whole step
 (forward + backward), summed over ranks, with inputs resident in HBM: K steps
-back to back between two CUDA events.  Inputs are larger than L2: three copies
+back to back between two CUDA events, the K steps captured once into a CUDA
+graph and replayed (the library's calls are capturable; the replay runs every
+step's kernels, without a host launch between them; the same K steps launched
+eagerly are reported under `eager`).  Inputs are larger than L2: three copies
 are used in rotation, so each kernel call reads a set last touched three calls
 earlier and streams it from HBM (no flush).  `fwd` and `bwd` time each pass
 alone the same way (K calls back to back).  `e2e` is the same metric
@@ -218,25 +221,40 @@ class Resident:
         self.dsc = torch.empty((c.n_tokens, C), dtype=torch.int16, device=dev)
         self.dape = torch.empty((c.ratio, C), dtype=torch.float32, device=dev)
 
+    # The calls run on torch's current stream: the timing stream, or the capture
+    # stream while a region is captured into a CUDA graph.
     def fwd(self, k):
         c = self.c
         kv, sc, _ = self.sets[k % INPUT_SETS]
         self.csa.csa_compress_fwd(kv, sc, self.ape, self.cu, self.cc, c.n_seg, c.ratio, c.coff, c.head_dim,
-                                  c.capacity, self.out, self.stream)
+                                  c.capacity, self.out, None)
 
     def bwd(self, k):
         c = self.c
         kv, sc, g = self.sets[k % INPUT_SETS]
         self.csa.csa_compress_bwd(kv, sc, self.ape, self.cu, self.cc, c.n_seg, c.ratio, c.coff, c.head_dim,
-                                  c.capacity, c.n_tokens, g, self.dkv, self.dsc, self.dape, self.stream)
+                                  c.capacity, c.n_tokens, g, self.dkv, self.dsc, self.dape, None)
 
     def step(self, i):
         self.fwd(2 * i)
         self.bwd(2 * i + 1)
 
-    def region(self, fn, k):
-        """k calls fn(0..k-1) back to back between two events: mean ms per call."""
+    def region(self, fn, k, graph=True):
+        """k calls fn(0..k-1) back to back between two events: mean ms per call.
+        graph: the k calls are captured once into a CUDA graph (after the warm-up
+        the caller has done), the graph replayed once untimed, then the timed
+        replay runs every call's kernels again -- the same work as the eager loop,
+        without a host launch between kernels."""
         import torch
+        g = None
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(k):
+                    fn(i)
+            g.replay()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         if self.world > 1:
@@ -244,8 +262,11 @@ class Resident:
             dist.barrier()
         torch.cuda.synchronize()
         e0.record(self.stream)
-        for i in range(k):
-            fn(i)
+        if g is not None:
+            g.replay()
+        else:
+            for i in range(k):
+                fn(i)
         e1.record(self.stream)
         torch.cuda.synchronize()
         if self.world > 1:
@@ -267,7 +288,7 @@ def run_ours(args, rank, world, local_rank):
         fn = r.fwd if args.pass_only == "fwd" else r.bwd
         for i in range(args.warmup):
             fn(i)
-        ms = r.region(fn, args.steps)
+        ms = r.region(fn, args.steps, graph=False)  # launched one by one: each launch visible to a profiler
         return c, None, ms, None, None, None, {"pass_only": args.pass_only}
 
     sampler = ClockSampler(local_rank) if rank == 0 and not args.no_clocks else None
@@ -282,19 +303,22 @@ def run_ours(args, rank, world, local_rank):
         n += 1
         if n % 10 == 0:
             torch.cuda.synchronize()
-    # the timed region: K whole steps (forward + backward)
+    # the timed region: K whole steps (forward + backward), replayed from a CUDA graph
     ms_step = r.region(r.step, args.steps)
     # each pass alone, K calls back to back (its average launch duration)
     ms_fwd = r.region(r.fwd, args.steps)
     ms_bwd = r.region(r.bwd, args.steps)
-    ms_step, ms_fwd, ms_bwd = max_over_ranks([ms_step, ms_fwd, ms_bwd])
+    # the same three regions launched eagerly from the host, for comparison
+    eager = [r.region(fn, args.steps, graph=False) for fn in (r.step, r.fwd, r.bwd)]
+    ms_step, ms_fwd, ms_bwd, *eager = max_over_ranks([ms_step, ms_fwd, ms_bwd] + eager)
     del r
     extra = {}
     if args.workload == DEFAULT_WORKLOAD and not args.no_extra:
-        extra = run_extra(args, csa, dev, stream, rank, world)
+        extra["workloads"] = run_extra(args, csa, dev, stream, rank, world)
     clocks = sampler.stop() if sampler else None
 
     e2e = None if args.no_e2e else run_e2e(args, c, csa, dev, stream, world)
+    extra["eager_ms"] = {"step": eager[0], "fwd": eager[1], "bwd": eager[2]}
     return c, ms_step, ms_fwd, ms_bwd, clocks, e2e, extra
 
 
@@ -544,6 +568,8 @@ def main():
                    "capacity": c.capacity,
                    "l2": "inputs larger than L2: %d rotating input sets, each call reads a set last touched "
                          "3 calls earlier; no flush" % INPUT_SETS,
+                   "launch": "each timed region of K calls captured once into a CUDA graph and replayed "
+                             "(after the warm-up); eager timings under 'eager'",
                    "inputs": "bf16 kv/score/grad_out, fp32 ape; fp32 arithmetic"},
         "fwd": {"ms": ms_fwd, "tokens_per_s": world * tokens / (ms_fwd * 1e-3), "bytes": fwd_b,
                 "gbs": gbs(fwd_b, ms_fwd), "frac_of_peak": gbs(fwd_b, ms_fwd) / peak},
@@ -556,8 +582,11 @@ def main():
         "gpu_launches": 3 * args.steps,
         "clocks": clocks,
     }
-    if extra:
-        line["workloads"] = extra
+    if extra.get("workloads"):
+        line["workloads"] = extra["workloads"]
+    line["eager"] = {"ms_per_step": extra["eager_ms"]["step"], "fwd_ms": extra["eager_ms"]["fwd"],
+                     "bwd_ms": extra["eager_ms"]["bwd"],
+                     "note": "the same K calls launched one by one from the host (no CUDA graph)"}
     if e2e is not None:
         line["e2e"] = e2e
     if not args.no_cpu_baseline:

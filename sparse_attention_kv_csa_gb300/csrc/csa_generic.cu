@@ -358,7 +358,8 @@ struct GsMeta {
     int row;
     int real;
     int first;
-    int pad[2];
+    int last;  // the last block of its segment (from the producer's row cursor)
+    int pad;
 };
 
 struct GsSmem {
@@ -416,6 +417,7 @@ __device__ void gs_produce(const GsArgs &a, const GsSmem &s, const CUtensorMap *
         m.row = row;
         m.real = rm.real;
         m.first = rm.first;
+        m.last = rm.real && row + 1 == cur.hi;
         const bool load = BWD ? rm.real : true;
         const int p0 = (g.coff == 2 && rm.first) ? 1 : 0;
         const uint32_t bytes = load ? (uint32_t)(g.coff - p0) * 2u * part_bytes + (BWD ? kGsTile * 2u : 0u) : 0u;
@@ -675,7 +677,7 @@ __global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_addr(&s.empty[st]));
-            if (m.row + 1 == __ldg(g.cc + m.seg + 1)) {  // last block of its segment
+            if (m.last) {  // last block of its segment
                 if (g.coff == 2)  // own block's first-half columns: read by no row
                     gs_zero(g, dkv, dscore, C, j0, m.base, m.base + g.ratio, n_tokens, false);
                 int64_t next = n_tokens;

@@ -169,7 +169,8 @@ struct StageMeta {
     int row;
     int real;
     int first;
-    int pad[2];
+    int last;  // the last block of its segment (from the producer's row cursor)
+    int pad;
 };
 
 // Window position k reads part p = k / RATIO, token i = k % RATIO of the part.
@@ -244,6 +245,7 @@ __device__ void produce(const StreamArgs &a, const Smem &s, const CUtensorMap *t
         m.row = row;
         m.real = rm.real;
         m.first = rm.first;
+        m.last = rm.real && row + 1 == cur.hi;
         const bool load = BWD ? rm.real : true;
         const int p0 = (COFF == 2 && rm.first) ? 1 : 0;
         const uint32_t bytes =
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(Cols<NP>::MAX_THREADS) bwd_stream_kernel(Strea
                     st_np(dscore + gi, dsw);
                 }
             }
-            if (m.row + 1 == __ldg(a.cc + m.seg + 1)) {  // last block of its segment
+            if (m.last) {  // last block of its segment
                 if (COFF == 2) {
                     for (int i = 0; i < RATIO; ++i) {
                         const int64_t tok = m.base + i;
