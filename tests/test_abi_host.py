@@ -90,3 +90,25 @@ def test_check_support_surface():
     assert csa.csa_check_support(129, 1, 512, 1000, 1) == 2   # no kernel beyond 128
     assert csa.csa_check_support(7, 2, 500, 100, 1) == 2      # head_dim % 8
     assert csa.csa_check_support(128, 1, 96, 1000, 1) == 2    # ratio 128: head_dim % 64
+
+
+@pytest.mark.parametrize("args,status", [
+    ((4, 3, 512, 8), 1), ((0, 2, 512, 8), 1), ((4, 2, 0, 8), 1), ((4, 2, 512, -1), 1),
+    ((129, 1, 512, 8), 2), ((4, 2, 60, 8), 2), ((128, 1, 96, 8), 2), ((4, 2, 512, 1 << 30), 4),
+])
+def test_grad_ape_order_rejects_bad_shapes_before_any_device_query(args, status):
+    with pytest.raises(csa.CSAError) as ei:
+        csa.csa_grad_ape_order(*args)
+    assert ei.value.status == status
+
+
+def test_grad_ape_order_needs_a_device_but_fails_cleanly_without_one():
+    import torch
+    if torch.cuda.is_available():
+        g = csa.csa_grad_ape_order(4, 2, 512, 8256)
+        assert g["kind"] == "row_blocks" and g["final_ranges"] == 32
+        assert g["partials"] * g["cluster"] == g["blocks"]
+    else:
+        with pytest.raises(csa.CSAError) as ei:
+            csa.csa_grad_ape_order(4, 2, 512, 8256)
+        assert ei.value.status == 5  # CSA_ERR_CUDA: no device to query
