@@ -143,8 +143,9 @@ CSA_API int csa_compress_bwd(const void *kv, const void *score, const float *ape
  * could block, a plug-in that may not use the CUDA allocator.
  *
  * Same arguments, results and errors as csa_compress_bwd (bitwise the same
- * outputs, but see below for the chunked windows' grad_ape), except that the grad_ape partial sums go to a fixed 6 MiB array in
- * the library's device code instead of the library's memory pool.  That array
+ * outputs, but see below for the chunked windows' grad_ape), except that the
+ * grad_ape partial sums go to a fixed 6 MiB array in the library's device code
+ * instead of the library's memory pool.  That array
  * occupies 6 MiB on every GPU that loads the library, until the process exits.
  * Where the regular backward's grid would need more partial storage than the
  * array holds, the chunked windows (ratio 128, and other ratios with more than 64

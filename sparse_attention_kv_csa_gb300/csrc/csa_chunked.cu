@@ -9,13 +9,14 @@
 // rows b, b + gridDim.x, ...  One producer warp streams, per row, the window's
 // [ratio tokens x TC columns] boxes of kv and score (one box per array and part)
 // with 2-D TMA tensor copies into a shared-memory ring tracked by mbarriers (and,
-// in the backward, the grad_out row with a bulk copy).  NC chunks (16 for windows
-// of up to 128 positions, 32 up to 256): a thread owns a group g of 4 columns and
+// in the backward, the grad_out row with a bulk copy).  NC chunks (12 to 32,
+// covering the window): a thread owns a group g of 4 columns and
 // a chunk c, whose window positions are k = c, c + NC, c + 2*NC, ... (8 of them;
 // those at or past the window's end are skipped), so that the lanes of a warp
 // read consecutive box rows (no bank conflicts) and each thread's APE values stay
 // in registers.  Ratio 128 is compiled with the ratio as a constant; the other
-// ratios take it at run time.
+// ratios take it at run time, with the fewest chunks (a multiple of the warps'
+// chunk count) that cover the window.
 //
 // Order of the arithmetic (the page's ratio-128 family: a deterministic chunked
 // order, checked against the plain sequential oracle by tolerance; the library
@@ -76,10 +77,17 @@ struct Geo {
     static constexpr int CT = CW * 32;        // consumer threads
     static constexpr int THREADS = CT + 32;   // + one producer warp
     static constexpr int RS = TC + 4;         // row stride of the merge buffers
-    // resident blocks per SM the registers are sized for: three of the four-warp
-    // blocks (ratio 64 with coff 2: forward 32.1 -> 29.7 us, backward 66.5 -> 64.8
-    // us at 8 x 4096 tokens, head_dim 512), else two
-    static constexpr int MIN_BLOCKS = CW == 4 ? 3 : 2;
+    // The final merge: TPC consecutive threads per tile column (a power of two, so
+    // that a fixed xor tree joins them within a warp), each adding WPT warp sums;
+    // the threads past MT = TPC * TC take no part in it.
+    static constexpr int TPC = (CW % 8 == 0 && 8 * TC <= CT) ? 8 : (CW % 4 == 0 && 4 * TC <= CT) ? 4
+                             : (CW % 2 == 0 && 2 * TC <= CT) ? 2 : 1;
+    static constexpr int WPT = CW / TPC;
+    static constexpr int MT = TPC * TC;
+    // resident blocks per SM the registers are sized for: three of the blocks with
+    // at most four consumer warps (ratio 64 with coff 2: forward 32.1 -> 29.7 us,
+    // backward 66.5 -> 64.8 us at 8 x 4096 tokens, head_dim 512), else two
+    static constexpr int MIN_BLOCKS = CW <= 4 ? 3 : 2;
     // coff 1: each warp's terms are taken relative to the warp's own maximum and
     // the merge rescales them to the row's (one block barrier fewer per row;
     // ratio 128 backward 100.6 -> 97.4 us, ratio 96 forward / backward 26.4 / 63.2
@@ -437,18 +445,19 @@ __device__ __forceinline__ bool ch_pool(const Win<COFF, NCB, RC> &w, const ChSme
     return true;
 }
 
-// The fixed-order merge of the warp sums, spread over all consumer threads: TPC
-// consecutive threads own tile column j; each adds its warps' sums in ascending
-// order, then the TPC partial sums meet in a fixed xor-shuffle tree, so every one
-// of them ends with the same den and num of column j.
+// The fixed-order merge of the warp sums, spread over the first MT consumer threads:
+// TPC consecutive threads own tile column j; each adds its WPT warps' sums in
+// ascending order, then the TPC partial sums meet in a fixed xor-shuffle tree, so
+// every one of them ends with the same den and num of column j.  Only threads
+// below MT may call it.
 template <int COFF, int NCB>
 __device__ __forceinline__ void ch_final(const ChSmem<COFF, NCB> &s, int buf, int &j, float &den, float &num,
                                          float *scale)
 {
     using G = Geo<COFF, NCB>;
-    constexpr int TPC = G::CT / G::TC;  // threads per column
-    constexpr int WPT = G::CW / TPC;    // warp sums per thread
-    static_assert(TPC * G::TC == G::CT && WPT * TPC == G::CW, "merge split");
+    constexpr int TPC = G::TPC;  // threads per column
+    constexpr int WPT = G::WPT;  // warp sums per thread
+    static_assert(WPT * TPC == G::CW && G::MT <= G::CT && 32 % TPC == 0, "merge split");
     j = (int)threadIdx.x / TPC;
     const int q = (int)threadIdx.x % TPC;
     const float *dn = s.den + (size_t)buf * G::CW * G::RS + q * WPT * G::RS + j;
@@ -567,10 +576,12 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, Geo<COFF, NCB>::MIN_B
         {
             int j;
             float den, num;
-            ch_final<COFF, NCB>(s, buf, j, den, num, nullptr);
-            if (threadIdx.x % (G::CT / G::TC) == 0) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, recip_den(den)));
-                out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
+            if (threadIdx.x < G::MT) {
+                ch_final<COFF, NCB>(s, buf, j, den, num, nullptr);
+                if (threadIdx.x % G::TPC == 0) {
+                    const __nv_bfloat16 h = __float2bfloat16_rn(__fmul_rn(num, recip_den(den)));
+                    out[(int64_t)row * a.head_dim + c0 + j] = *reinterpret_cast<const uint16_t *>(&h);
+                }
             }
         }
         buf ^= 1;
@@ -690,11 +701,13 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF> ? Geo<
             {
                 int j;
                 float den, num;
-                ch_final<COFF, NCB>(s, buf, j, den, num, G::LOCAL ? fin + 2 * G::TC : nullptr);
-                if (threadIdx.x % (G::CT / G::TC) == 0 && m.real) {
-                    const float inv = recip_den(den);
-                    fin[j] = inv;
-                    fin[G::TC + j] = __fmul_rn(num, inv);  // o
+                if (threadIdx.x < G::MT) {
+                    ch_final<COFF, NCB>(s, buf, j, den, num, G::LOCAL ? fin + 2 * G::TC : nullptr);
+                    if (threadIdx.x % G::TPC == 0 && m.real) {
+                        const float inv = recip_den(den);
+                        fin[j] = inv;
+                        fin[G::TC + j] = __fmul_rn(num, inv);  // o
+                    }
                 }
             }
             named_barrier(1, G::CT);
@@ -936,15 +949,25 @@ bool chunked_supported(int ratio, int coff, int head_dim)
 }
 
 // The kernel instance for a shape: ratio 128 with the ratio as a constant (16
-// chunks for coff 1, 32 for coff 2); other ratios at run time, 16 chunks for
-// windows of up to 128 positions, 32 up to 256.
+// chunks for coff 1, 32 for coff 2); other ratios at run time with the fewest
+// chunks of 8 positions that cover the window, in steps of whole consumer warps
+// (coff 1: 12 or 16 chunks, windows up to 96 or 128; coff 2: 12, 16, 20, 24, 28
+// or 32 chunks, windows up to 96 ... 256), so that no warp holds only positions
+// past the window.
 #define CSA_CHUNK_DISPATCH(FN, ...)                                                         \
     do {                                                                                    \
         if (ratio == 128)                                                                   \
             return coff == 2 ? FN<2, 32, 128>(__VA_ARGS__) : FN<1, 16, 128>(__VA_ARGS__);   \
         if (coff == 1)                                                                      \
-            return FN<1, 16, 0>(__VA_ARGS__);                                               \
-        return 2 * ratio <= 128 ? FN<2, 16, 0>(__VA_ARGS__) : FN<2, 32, 0>(__VA_ARGS__);    \
+            return ratio <= 96 ? FN<1, 12, 0>(__VA_ARGS__) : FN<1, 16, 0>(__VA_ARGS__);     \
+        switch ((2 * ratio + 31) / 32) {                                                    \
+        case 3: return FN<2, 12, 0>(__VA_ARGS__);                                           \
+        case 4: return FN<2, 16, 0>(__VA_ARGS__);                                           \
+        case 5: return FN<2, 20, 0>(__VA_ARGS__);                                           \
+        case 6: return FN<2, 24, 0>(__VA_ARGS__);                                           \
+        case 7: return FN<2, 28, 0>(__VA_ARGS__);                                           \
+        default: return FN<2, 32, 0>(__VA_ARGS__);                                          \
+        }                                                                                   \
     } while (0)
 
 cudaError_t launch_fwd_chunked(const FwdParams &p, unsigned *status, cudaStream_t st)

@@ -648,11 +648,11 @@ __global__ void __launch_bounds__(Cols<NP>::MAX_THREADS) bwd_stream_kernel(Strea
     cluster.sync();
 }
 
-// Widest tile of at most 512 columns (whole consumer warps of cpw columns) that
+// Widest tile of at most max_tc columns (whole consumer warps of cpw columns) that
 // divides head_dim.
-int tile_cols(int head_dim, int cpw)
+int tile_cols(int head_dim, int cpw, int max_tc)
 {
-    for (int w = 512 / cpw; w >= 1; --w)
+    for (int w = max_tc / cpw; w >= 1; --w)
         if (head_dim % (w * cpw) == 0)
             return w * cpw;
     return 0;
@@ -674,7 +674,10 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     StreamPlan pl;
     pl.np = head_dim % 128 == 0 ? 2 : 1;
     const int cpw = 64 * pl.np;  // columns per consumer warp
-    pl.tc = tile_cols(head_dim, cpw);
+    // tiles of up to 512 columns; 256 for the own-block backward (coff 1, head_dim
+    // 512: 58.3 -> 55.6 us at 16 x 4096 tokens; the forward and the coff-2
+    // backward measured slower with the narrower tile)
+    pl.tc = tile_cols(head_dim, cpw, bwd && coff == 1 ? 256 : 512);
     pl.tiles = head_dim / pl.tc;
     // Up to four consumer warps per block: tiles of one or two warps take several
     // rows at once (more would leave the block's one producer behind).

@@ -28,8 +28,11 @@ def layouts(r):
     return [[19 * r + 3, r, 5, 30 * r + 1], [r - 1], [r], [r + 1, 0, 16 * r], [24 * r], [3, 21 * r + 7, 2]]
 
 
-CASES = [(2, 33), (2, 40), (2, 48), (2, 63), (2, 64), (2, 65), (2, 96), (2, 127),
-         (1, 65), (1, 80), (1, 100), (1, 127)]
+# every chunk-count bucket and its edges: coff 2 with windows up to 96 / 128 / 160 /
+# 192 / 224 / 256 positions (12 ... 32 chunks), coff 1 up to 96 / 128 (12 / 16)
+CASES = [(2, 33), (2, 40), (2, 48), (2, 49), (2, 63), (2, 64), (2, 65), (2, 80), (2, 81), (2, 96),
+         (2, 100), (2, 112), (2, 113), (2, 127),
+         (1, 65), (1, 80), (1, 96), (1, 97), (1, 100), (1, 127)]
 
 
 @pytest.mark.parametrize("coff,ratio", CASES)
