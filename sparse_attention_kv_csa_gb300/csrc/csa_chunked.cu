@@ -216,17 +216,20 @@ __device__ void ch_produce(const ChArgs &a, const ChSmem<COFF, NCB> &s, const CU
     const int R = w.ratio();
     int issued = 0, st = 0;
     uint32_t ph = 0;
+    RowCursor cur;
+    cursor_init(cur, a.cc, a.n_seg);
     for (int row = row0; row < rend; row += rstride) {
+        // the row's map first: its loads (if any) overlap the wait for a free slot
+        const RowMap rm = cursor_map(cur, row, a.cu, a.cc, a.n_seg, R);
         if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
             break;
-        const RowMap rm = map_row(row, a.cu, a.cc, a.n_seg, R);
         Meta &m = s.meta[st];
         m.base = rm.base;
         m.seg = rm.seg;
         m.row = row;
         m.real = rm.real;
         m.first = rm.first;
-        m.last = rm.real && row + 1 == __ldg(a.cc + rm.seg + 1);
+        m.last = rm.real && row + 1 == cur.hi;
         const bool load = BWD ? rm.real : true;
         const int p0 = (COFF == 2 && rm.first) ? 1 : 0;
         const uint32_t bytes =

@@ -203,8 +203,9 @@ __device__ __forceinline__ RowMap map_row(int r, const int32_t *__restrict__ cu,
 
 // Row -> window map for one thread's increasing rows.  The offsets of the
 // current segment stay in registers, so the next row of the same segment costs
-// no load; the binary search (dependent loads, slow under a full memory system)
-// runs once per segment change.  Same result as map_row.
+// no load; a row a few segments further costs one load per boundary stepped
+// over; only a longer jump takes the binary search (dependent loads, slow under a
+// full memory system).  Same result as map_row.
 struct RowCursor {
     int r0, r1;            // real rows: [cc[0], cc[n_seg])
     int lo, hi, tok;       // current segment: rows [lo, hi), first token tok
@@ -231,9 +232,25 @@ __device__ __forceinline__ RowMap cursor_map(RowCursor &c, int r, const int32_t 
     if (r < c.r0 || r >= c.r1)
         return m;
     if (c.seg < 0 || r < c.lo || r >= c.hi) {
-        c.seg = find_segment(cc, n_seg, r);
-        c.lo = __ldg(cc + c.seg);
-        c.hi = __ldg(cc + c.seg + 1);
+        // Rows only increase: step over up to four segment boundaries (one load
+        // each) before falling back to the binary search.  r < r1 = cc[n_seg]
+        // keeps every load inside cc.
+        int s = c.seg, lo = c.lo, hi = c.hi;
+        if (s >= 0 && r >= hi)
+            for (int k = 0; k < 4 && r >= hi; ++k) {
+                ++s;
+                lo = hi;
+                hi = __ldg(cc + s + 1);
+            }
+        if (s >= 0 && r >= lo && r < hi) {
+            c.seg = s;
+            c.lo = lo;
+            c.hi = hi;
+        } else {
+            c.seg = find_segment(cc, n_seg, r);
+            c.lo = __ldg(cc + c.seg);
+            c.hi = __ldg(cc + c.seg + 1);
+        }
         c.tok = __ldg(cu + c.seg);
     }
     const int b = r - c.lo;

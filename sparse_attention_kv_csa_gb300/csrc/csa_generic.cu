@@ -408,9 +408,10 @@ __device__ void gs_produce(const GsArgs &a, const GsSmem &s, const CUtensorMap *
     RowCursor cur;
     cursor_init(cur, g.cc, g.n_seg);
     for (int row = row0; row < rend; row += rstride) {
+        // the row's map first: its loads (if any) overlap the wait for a free slot
+        const RowMap rm = cursor_map(cur, row, g.cu, g.cc, g.n_seg, g.ratio);
         if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
             break;
-        const RowMap rm = cursor_map(cur, row, g.cu, g.cc, g.n_seg, g.ratio);
         GsMeta &m = s.meta[st];
         m.base = rm.base;
         m.seg = rm.seg;

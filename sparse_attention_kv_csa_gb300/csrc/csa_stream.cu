@@ -236,9 +236,10 @@ __device__ void produce(const StreamArgs &a, const Smem &s, const CUtensorMap *t
     RowCursor cur;
     cursor_init(cur, a.cc, a.n_seg);
     for (int row = row0; row < rend; row += rstride) {
+        // the row's map first: its loads (if any) overlap the wait for a free slot
+        const RowMap rm = cursor_map(cur, row, a.cu, a.cc, a.n_seg, RATIO);
         if (!mbar_wait(smem_addr(&s.empty[st]), ph ^ 1u, a.status))
             break;
-        const RowMap rm = cursor_map(cur, row, a.cu, a.cc, a.n_seg, RATIO);
         StageMeta &m = s.meta[st];
         m.base = rm.base;
         m.seg = rm.seg;

@@ -176,12 +176,13 @@ def test_small_layouts_bitwise(csa, coff, head_dim, li):
 
 
 @pytest.mark.parametrize("coff", [1, 2])
-@pytest.mark.parametrize("head_dim", [128, 256, 640])
+@pytest.mark.parametrize("head_dim", [128, 256, 640, 1024])
 @pytest.mark.parametrize("li", [0, 2, 4, 6, 7, 9])
 def test_stream_row_lanes_bitwise(csa, coff, head_dim, li):
-    """Tiles of 128 and 256 columns (head_dim 128, 640: 128; 256: 256) run two
-    rows of a block side by side, and single-tile heads stage whole token rows;
-    any layout, any number of rows per block, gives the oracle's bits."""
+    """Tiles of 128 and 256 columns (head_dim 128, 640: 128; 256: 256; the coff-1
+    backward at head_dim 1024: four tiles of 256) run two rows of a block side by
+    side, and single-tile heads stage whole token rows; any layout, any number of
+    rows per block, gives the oracle's bits."""
     lens = LAYOUTS[li] + [4 * 777 + 2]
     extra = (0, 1, 5)[li % 3]
     leading = (0, 3)[li % 2]
