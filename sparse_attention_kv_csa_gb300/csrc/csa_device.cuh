@@ -70,23 +70,33 @@ __device__ __forceinline__ float recip_den(float d)
 // ------------------------------------------------------------------ exp
 // e^x for x <= 0 (or NaN), the library's own: Cody-Waite reduction (Cody and
 // Waite, "Software Manual for the Elementary Functions", 1980) x = n ln2 + r with
-// ln2 split in two parts, |r| <= ln2/2; e^r by its degree-7 Taylor polynomial in
-// Horner form; 2^n put into the exponent field.  Results below 2^-126.5 are +0
-// (n = -127 gives a zero scale); NaN propagates.  Constants from their definitions:
+// ln2 split in two parts, |r| <= h = ln2/2; e^r by a degree-6 polynomial in Horner
+// form; 2^n put into the exponent field.  Results below 2^-126.5 are +0 (n = -127
+// gives a zero scale); NaN propagates.  Constants from their definitions:
 //   kLog2e = 1/ln2 to fp32; kLn2Hi = ln2 cut to a 16-bit significand (so n*kLn2Hi
 //   is exact); kLn2Lo = ln2 - kLn2Hi to fp32; kRound = 1.5*2^23 (adding it leaves
-//   nearest(y) in the low significand bits); kInvFact[k] = 1/k! to fp32.
+//   nearest(y) in the low significand bits).
+// The polynomial is the degree-7 Taylor polynomial of e^r with its r^7 term
+// economized over |r| <= h (Lanczos, "Applied Analysis", 1956): with x = r/h and
+// the Chebyshev polynomial T7(x) = 64x^7 - 112x^5 + 56x^3 - 7x,
+//   r^7 = h^7 (T7(x) + 112x^5 - 56x^3 + 7x) / 64,
+// and dropping T7 (|T7| <= 1) moves 1/7! onto r^5, r^3 and r:
+//   kC5 = 1/5! + (1/7!)(112/64)h^2,  kC3 = 1/3! - (1/7!)(56/64)h^4,
+//   c1 = 1 + (1/7!)(7/64)h^6 = 1 in fp32 (the change is below half an ulp),
+// the others 1/k!; computed in double, rounded to fp32.  Error about 7e-9
+// relative (h^7/(64 7!) + h^8/8!), as small as the degree-7 Taylor polynomial's.
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kLn2Hi = 0.693145751953125f;
 constexpr float kLn2Lo = 1.42860682030941723212e-6f;
 constexpr float kRound = 12582912.0f;
 constexpr float kExpFloor = -88.0f;
-constexpr float kInvFact2 = 1.0f / 2.0f;
-constexpr float kInvFact3 = 1.0f / 6.0f;
-constexpr float kInvFact4 = 1.0f / 24.0f;
-constexpr float kInvFact5 = 1.0f / 120.0f;
-constexpr float kInvFact6 = 1.0f / 720.0f;
-constexpr float kInvFact7 = 1.0f / 5040.0f;
+constexpr double kHalfLn2 = 0.69314718055994530942 / 2.0;
+constexpr double kHalfLn2Sq = kHalfLn2 * kHalfLn2;
+constexpr float kC2 = (float)(1.0 / 2.0);
+constexpr float kC3 = (float)(1.0 / 6.0 - (1.0 / 5040.0) * (56.0 / 64.0) * (kHalfLn2Sq * kHalfLn2Sq));
+constexpr float kC4 = (float)(1.0 / 24.0);
+constexpr float kC5 = (float)(1.0 / 120.0 + (1.0 / 5040.0) * (112.0 / 64.0) * kHalfLn2Sq);
+constexpr float kC6 = (float)(1.0 / 720.0);
 
 __device__ __forceinline__ float2 exp2lanes(float2 x)
 {
@@ -96,11 +106,10 @@ __device__ __forceinline__ float2 exp2lanes(float2 x)
     const float2 n = add2(t, splat(-kRound));                  // n, exact
     float2 r = fma2(n, splat(-kLn2Hi), x);
     r = fma2(n, splat(-kLn2Lo), r);
-    float2 p = fma2(splat(kInvFact7), r, splat(kInvFact6));
-    p = fma2(p, r, splat(kInvFact5));
-    p = fma2(p, r, splat(kInvFact4));
-    p = fma2(p, r, splat(kInvFact3));
-    p = fma2(p, r, splat(kInvFact2));
+    float2 p = fma2(splat(kC6), r, splat(kC5));
+    p = fma2(p, r, splat(kC4));
+    p = fma2(p, r, splat(kC3));
+    p = fma2(p, r, splat(kC2));
     p = fma2(p, r, splat(1.0f));
     p = fma2(p, r, splat(1.0f));
     // bits(t) = bits(kRound) + n; bits(kRound) << 23 vanishes mod 2^32, so

@@ -36,7 +36,9 @@ MUTATIONS = {
     "padding_rows_carry_gradient": ("            continue; /* padding rows: incoming gradient ignored */",
                                     "            ; /* mutated */"),
     "exp_drops_ln2_low_part": ("    r = fmaf(nf, -CSA_LN2_LO, r);", "    r = fmaf(nf, 0.0f, r);"),
-    "exp_wrong_taylor_coefficient": ("1.0f / 720.0f", "1.0f / 700.0f"),
+    "exp_wrong_polynomial_coefficient": ("(float)(1.0 / 720.0)", "(float)(1.0 / 700.0)"),
+    "exp_economization_dropped": ("(float)(1.0 / 120.0 + (1.0 / 5040.0) * (112.0 / 64.0) * CSA_H2)",
+                                  "(float)(1.0 / 120.0)"),
     "bf16_rounds_ties_away": ("    u += 0x7fffu + ((u >> 16) & 1u);", "    u += 0x8000u;"),
 }
 
