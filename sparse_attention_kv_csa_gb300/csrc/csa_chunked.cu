@@ -56,14 +56,16 @@ namespace {
 
 constexpr int kKC = 8;  // window positions per chunk (per thread)
 
-// Backward layout per window form.  coff 1: APE and the kv words in registers,
-// the stage released as soon as it is read, one block per SM (registers), a
-// four-stage ring.  coff 2 (twice the column tiles per row): "lean" -- APE from a
-// shared tile, kv read again from the stage, which stays held until the row's
-// gradients are written -- so that two blocks fit per SM.  Each measured faster
-// for its form on GB300 at ratio 128.
-template <int COFF>
-constexpr bool kBwdLean = COFF == 2;
+// Backward layout per window form and chunk count.  Register-resident: APE and
+// the kv words in registers, the stage released as soon as it is read, one block
+// per SM (registers), a four-stage ring.  "Lean": APE from a shared tile, kv read
+// again from the stage, which stays held until the row's gradients are written,
+// so that two blocks fit per SM.  coff 2 (twice the column tiles per row) runs
+// lean; coff 1 runs lean up to 12 chunks, whose register-resident block has only
+// seven warps on its SM (ratio 96 at 8 x 6144 tokens, head_dim 512: 55.6 -> 46.7
+// us), and register-resident at 16 (ratio 128: 98.4 against 121 us lean).
+template <int COFF, int NCB>
+constexpr bool kBwdLean = COFF == 2 || NCB <= 12;
 
 // Block geometry for a form and a chunk count (the window's bucket).
 template <int COFF, int NCB>
@@ -611,14 +613,14 @@ __device__ __forceinline__ void ch_zero_tokens(uint16_t *dkv, uint16_t *dscore, 
 }
 
 template <int COFF, int NCB, int RC>
-__global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF> ? Geo<COFF, NCB>::MIN_BLOCKS : 1)
+__global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF, NCB> ? Geo<COFF, NCB>::MIN_BLOCKS : 1)
     bwd_chunk_kernel(ChArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
                      int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
                      uint16_t *__restrict__ dscore, float *__restrict__ partial)
 {
     using G = Geo<COFF, NCB>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    constexpr bool LEAN = kBwdLean<COFF>;
+    constexpr bool LEAN = kBwdLean<COFF, NCB>;
     unsigned char *smem_base = align_1k<LEAN>(smem_raw);
     const ChSmem<COFF, NCB> s = ch_carve<COFF, NCB>(smem_base, a.stages, a.stage_bytes, LEAN);
     const Win<COFF, NCB, RC> w(a);
@@ -827,7 +829,7 @@ ChPlan ch_plan(bool bwd, int ratio, int head_dim)
     ChPlan pl;
     pl.box_bytes = (ratio * G::TC * 2 + 127) / 128 * 128;
     pl.stage_bytes = (2 * COFF * pl.box_bytes + (bwd ? G::TC * 2 : 0) + 1023) / 1024 * 1024;
-    const bool tile = bwd && kBwdLean<COFF>;
+    const bool tile = bwd && kBwdLean<COFF, NCB>;
     // two blocks per SM (forward, lean backward): two stages; one block per SM
     // (register-resident backward): a four-stage ring fits
     pl.stages = bwd && !tile ? 4 : 2;
