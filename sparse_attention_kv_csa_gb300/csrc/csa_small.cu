@@ -538,22 +538,31 @@ __global__ void __launch_bounds__(kBwdThreads, kBwdMinBlocks)
 
 }  // namespace
 
-// grad_ape = the partials summed in a fixed order.  One warp per 4-float column:
-// lane l adds partials [l*P/32, (l+1)*P/32) in ascending order, then the 32
-// subtotals are combined by a fixed butterfly (xor 1, 2, 4, 8, 16).
+// grad_ape = the partials summed in a fixed order: range t of the 32 contiguous
+// ranges [t*P/32, (t+1)*P/32) is summed in ascending order from +0, then the 32
+// range sums are added pairwise, t with t^1, then with t^2, t^4, t^8, t^16.
+// A block takes kFinCols 4-float columns: a warp holds four ranges of them, eight
+// lanes per range on consecutive columns, so that each load of a partial is one
+// contiguous 128-byte piece; the range sums meet in shared memory, where one warp
+// runs the pairwise tree (a lane per float column).
 // Launched as a programmatic dependent of the backward kernel: griddepcontrol.wait
 // holds it until that grid has finished and its partials are visible (a plain
 // launch returns from the wait at once).
-__global__ void __launch_bounds__(256) dape_finalize_kernel(const float *__restrict__ partial,
-                                                            int n_partials, int64_t n,
-                                                            float *__restrict__ dape)
+constexpr int kFinCols = 8;
+constexpr int kFinThreads = 256;  // 8 warps x 4 ranges = 32 ranges
+static_assert(kFinThreads / 32 * (32 / kFinCols) == 32, "one range per thread");
+
+__global__ void __launch_bounds__(kFinThreads) dape_finalize_kernel(const float *__restrict__ partial,
+                                                                    int n_partials, int64_t n,
+                                                                    float *__restrict__ dape)
 {
+    __shared__ __align__(16) float sums[32 * kFinCols * 4];  // [range][float column]
     pdl_wait();
     pdl_trigger();
-    const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t i = gt >> 5;
-    const int t = (int)(gt & 31);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int t = warp * (32 / kFinCols) + lane / kFinCols;  // range
     const int64_t stride = n / 4;
+    const int64_t i = (int64_t)blockIdx.x * kFinCols + lane % kFinCols;  // 4-float column
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (i < stride) {
         const int lo = (int)((int64_t)t * n_partials / 32), hi = (int)((int64_t)(t + 1) * n_partials / 32);
@@ -580,25 +589,33 @@ __global__ void __launch_bounds__(256) dape_finalize_kernel(const float *__restr
             acc.w = __fadd_rn(acc.w, v.w);
         }
     }
+    // consecutive threads store consecutive 16-byte slots: no bank conflicts
+    reinterpret_cast<float4 *>(sums)[t * kFinCols + lane % kFinCols] = acc;
+    __syncthreads();
+    if (warp == 0 && lane < kFinCols * 4) {
+        float v[32];
 #pragma unroll
-    for (int m = 1; m < 32; m <<= 1) {
-        acc.x = __fadd_rn(acc.x, __shfl_xor_sync(0xffffffffu, acc.x, m));
-        acc.y = __fadd_rn(acc.y, __shfl_xor_sync(0xffffffffu, acc.y, m));
-        acc.z = __fadd_rn(acc.z, __shfl_xor_sync(0xffffffffu, acc.z, m));
-        acc.w = __fadd_rn(acc.w, __shfl_xor_sync(0xffffffffu, acc.w, m));
+        for (int r = 0; r < 32; ++r)
+            v[r] = sums[r * kFinCols * 4 + lane];
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1)  // level m: sums t and t^m (adjacent after the levels before)
+#pragma unroll
+            for (int r = 0; r < w; ++r)
+                v[r] = __fadd_rn(v[2 * r], v[2 * r + 1]);
+        const int64_t f = (int64_t)blockIdx.x * kFinCols * 4 + lane;
+        if (f < stride * 4)
+            dape[f] = v[0];
     }
-    if (i < stride && t == 0)
-        reinterpret_cast<float4 *>(dape)[i] = acc;
 }
 
 // ------------------------------------------------------------ launchers
 
 cudaError_t launch_dape_finalize(const float *partial, int n_partials, int64_t n, float *dape, cudaStream_t st)
 {
-    const int64_t threads = n / 4 * 32;
+    const int64_t blocks = (n / 4 + kFinCols - 1) / kFinCols;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((threads + 255) / 256), 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.gridDim = dim3((unsigned)(blocks > 0 ? blocks : 1), 1, 1);
+    cfg.blockDim = dim3(kFinThreads, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
