@@ -320,6 +320,30 @@ cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int b
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// [rows][C] bf16 seen as [rows][C / chunk_cols][chunk_cols]: a box {chunk_cols,
+// chunks, box_rows} at (0, col / chunk_cols, row) lands in shared memory as the
+// row-major [box_rows][chunks * chunk_cols] tile -- a tile wider than the 256
+// elements one box dimension may span, in one copy.  C must be a multiple of
+// chunk_cols.
+cudaError_t make_tensor_map_3d(CUtensorMap *m, const void *ptr, int64_t C, int chunk_cols, int chunks, int box_rows)
+{
+    cudaError_t e;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn(&e);
+    if (e != cudaSuccess)
+        return e;
+    if (chunk_cols <= 0 || C % chunk_cols != 0)
+        return cudaErrorInvalidValue;
+    const cuuint64_t dims[3] = {(cuuint64_t)chunk_cols, (cuuint64_t)(C / chunk_cols),
+                                (cuuint64_t)(((int64_t)1 << 31) / C)};
+    const cuuint64_t strides[2] = {(cuuint64_t)chunk_cols * 2, (cuuint64_t)C * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)chunk_cols, (cuuint32_t)chunks, (cuuint32_t)box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // The status word of the bounded waits, one per device: a word of this module's
 // device memory, so that neither entry point has to allocate it.
 static __device__ __align__(256) unsigned g_status_word[64];

@@ -76,7 +76,8 @@ struct StreamPlan {
     int tiles;           // head_dim / tc (gridDim.y)
     int row_lanes;       // rows in flight per block (tc / 128 column warps each)
     bool whole;          // stage whole token rows (one column tile)
-    bool tma;            // stage the tile with one 2-D TMA box per array and part (tc <= 256)
+    int tma;             // stage the tile with one TMA box per array and part: 0 no, 1 2-D (tc <= 256),
+                         // 2 3-D (tc a multiple of 256 above it)
     int threads;         // consumer warps + one producer warp, x 32
     int stage_bytes;     // bytes per ring stage
     int stages;          // ring depth
@@ -136,6 +137,7 @@ cudaError_t resident_blocks(const void *fn, int threads, size_t smem, int cluste
 // Tiled TMA map of a [rows, C] bf16 row-major tensor at ptr with [box_rows x
 // box_cols] boxes (no swizzle, 256-byte L2 promotion).
 cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int box_cols, int box_rows);
+cudaError_t make_tensor_map_3d(CUtensorMap *m, const void *ptr, int64_t C, int chunk_cols, int chunks, int box_rows);
 
 // The backward's kernel family and plan for one shape on the current device: one
 // computation shared by csa_compress_bwd, csa_compress_bwd_noalloc and

@@ -14,8 +14,8 @@
 //   * one producer warp: for each row, waits for a free stage of a shared-memory
 //     ring, then issues raw bulk copies (cp.async.bulk) of every window row the
 //     output row reads -- each (token, half) is one contiguous run of TC*2 bytes;
-//     whole token rows for a narrow single-tile head; one 2-D TMA box per array
-//     and part for the narrow tiles of a multi-tile head -- and, in the backward,
+//     whole token rows for a narrow single-tile head; one TMA box per array and
+//     part for the tiles of a wider head -- and, in the backward,
 //     the grad_out row; completion is counted in bytes on the stage's "full"
 //     mbarrier;
 //   * consumer warps: thread t owns columns [c0 + 2*NP*t, c0 + 2*NP*(t + 1)) of
@@ -42,6 +42,7 @@ namespace {
 
 // The plan's fixed choices (each measured on GB300 against its alternatives):
 constexpr int kWholeMaxD = 256;          // widest coff-2 head staged as whole token rows
+constexpr int kChunkCols = 256;          // widest span of one TMA box dimension
 constexpr int kFwdBudget = 64 * 1024;    // ring bytes of a forward block with four consumer warps
 constexpr int kBwdBudget = 64 * 1024;    // ... of a backward block
 constexpr int kBwdCluster = 2;           // backward blocks per cluster (grad_ape merged in DSMEM)
@@ -129,13 +130,16 @@ struct StreamArgs {
     int row_lanes;     // rows in flight per block: groups of tc / (32 * 2 * NP) warps
     int rw;            // elements per staged token row: tc, or C for whole rows
     int pcol;          // whole rows: head_dim (part p's data at column p * head_dim of a row); tiled: 0
-    int tma;           // tiled: one 2-D TMA box [RATIO tokens x tc] per array and part
+    int tma;           // tiled: 0 per-token copies; 1 one 2-D TMA box [RATIO tokens x tc] per array and
+                       // part; 2 one 3-D box [RATIO tokens x tc / 256 x 256] (tiles wider than 256)
 };
 
 // Staging of a window.  Tiled (rw = tc): per token of each part, the tile's
-// columns of that part, 2 * COFF * RATIO copies of tc elements -- or, for tiles
-// of at most 256 columns (the TMA box limit), one 2-D TMA box [RATIO tokens x tc]
-// per array and part, which lands in the same layout with 2 * COFF copies.  Whole rows (one
+// columns of that part, 2 * COFF * RATIO copies of tc elements -- or one TMA box
+// per array and part, which lands in the same layout with 2 * COFF copies: for
+// tiles of at most 256 columns (the limit of one box dimension) a 2-D box
+// [RATIO tokens x tc], for wider tiles (multiples of 256) a 3-D box over the rows
+// seen as [C / 256][256] chunks, [RATIO tokens x tc / 256 chunks x 256].  Whole rows (one
 // column tile, rw = C): per part, the RATIO whole token rows of its block, one
 // contiguous copy of RATIO * C elements per array; coff 2 then also stages the
 // half of each row the window does not use (the neighbouring row reads it), in
@@ -264,7 +268,19 @@ __device__ void produce(const StreamArgs &a, const Smem &s, const CUtensorMap *t
                     continue;
                 }
                 const int64_t col = (int64_t)p * a.head_dim + c0;
-                if (tma) {
+                // 3-D boxes once the ring has filled: while it fills, the per-token
+                // copies below deliver the first rows sooner (head_dim 512, coff 2,
+                // forward: 8 x 4096 tokens 27.2 -> 26.3 us against boxes from the
+                // start; 64 ragged segments 178.8 -> 170.5 us against per-token
+                // copies throughout).  x = 0: 16-byte aligned by construction.
+                if (tma && a.tma == 2 && issued >= a.stages) {
+                    tma_load_3d(dst + stage_offset<RATIO, COFF>(0, p, 0, tc), tm_kv, 0, (int)(col / kChunkCols),
+                                (int)tok0, fb);
+                    tma_load_3d(dst + stage_offset<RATIO, COFF>(1, p, 0, tc), tm_sc, 0, (int)(col / kChunkCols),
+                                (int)tok0, fb);
+                    continue;
+                }
+                if (tma && a.tma == 1) {
                     tma_load_2d(dst + stage_offset<RATIO, COFF>(0, p, 0, tc), tm_kv, (int)col, (int)tok0, fb);
                     tma_load_2d(dst + stage_offset<RATIO, COFF>(1, p, 0, tc), tm_sc, (int)col, (int)tok0, fb);
                     continue;
@@ -687,13 +703,15 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     const int warps = cols * pl.row_lanes;
     pl.threads = (warps + 1) * 32;
     // One column tile: whole token rows when the head is narrow enough (coff 2
-    // then also stages the unused half, in exchange for 8x fewer copies).  Several
-    // tiles of at most 256 columns (the TMA box limit): one 2-D TMA box per array
-    // and part (head_dim 640, coff 1: forward 34.0 -> 28.7 us against one bulk copy
-    // per token; a single coff-2 tile of 128 or 256 columns measured no faster
-    // with boxes than with whole rows).
+    // then also stages the unused half, in exchange for 8x fewer copies).  Other
+    // tiles: one TMA box per array and part, 2-D for tiles of at most 256 columns
+    // (head_dim 640, coff 1: forward 34.0 -> 28.7 us against one bulk copy per
+    // token; a single coff-2 tile of 128 or 256 columns measured no faster with
+    // boxes than with whole rows), 3-D for wider tiles that are multiples of 256
+    // (the 512-column tiles of head_dim 512, coff 2: four copies a row in place of
+    // sixteen per-token copies, whose issue bounds the producer).
     pl.whole = pl.tiles == 1 && (coff == 1 || head_dim <= kWholeMaxD);
-    pl.tma = !pl.whole && pl.tc <= 256;
+    pl.tma = pl.whole ? 0 : pl.tc <= kChunkCols ? 1 : pl.tc % kChunkCols == 0 ? 2 : 0;
     const int rw = pl.whole ? coff * head_dim : pl.tc;
     const int win = 2 * coff * ratio * rw * 2;
     pl.stage_bytes = ((bwd ? win + pl.tc * 2 : win) + 127) / 128 * 128;
@@ -737,13 +755,19 @@ StreamArgs stream_args(const void *kv, const void *score, const float *ape, cons
 {
     return StreamArgs{static_cast<const uint16_t *>(kv), static_cast<const uint16_t *>(score), ape, cu, cc, n_seg,
                       head_dim, capacity, pl.stages, pl.stage_bytes, status, pl.tc, pl.row_lanes,
-                      pl.whole ? coff * head_dim : pl.tc, pl.whole ? head_dim : 0, pl.tma ? 1 : 0};
+                      pl.whole ? coff * head_dim : pl.tc, pl.whole ? head_dim : 0, pl.tma};
 }
 
 template <int RATIO>
 cudaError_t stream_maps(const StreamPlan &pl, const void *kv, const void *score, int64_t C, CUtensorMap *mk,
                         CUtensorMap *ms)
 {
+    if (pl.tma == 2) {
+        cudaError_t e = make_tensor_map_3d(mk, kv, C, kChunkCols, pl.tc / kChunkCols, RATIO);
+        if (e == cudaSuccess)
+            e = make_tensor_map_3d(ms, score, C, kChunkCols, pl.tc / kChunkCols, RATIO);
+        return e;
+    }
     if (!pl.tma)
         return cudaSuccess;
     cudaError_t e = make_tensor_map_2d(mk, kv, C, pl.tc, RATIO);
