@@ -77,7 +77,7 @@ struct StreamPlan {
     int row_lanes;       // rows in flight per block (tc / 128 column warps each)
     bool whole;          // stage whole token rows (one column tile)
     int tma;             // stage the tile with one TMA box per array and part: 0 no, 1 2-D (tc <= 256),
-                         // 2 3-D (tc a multiple of 256 above it)
+                         // 2 3-D (coff 2, tc a multiple of 256 above it)
     int threads;         // consumer warps + one producer warp, x 32
     int stage_bytes;     // bytes per ring stage
     int stages;          // ring depth

@@ -143,8 +143,10 @@ struct StreamArgs {
 // column tile, rw = C): per part, the RATIO whole token rows of its block, one
 // contiguous copy of RATIO * C elements per array; coff 2 then also stages the
 // half of each row the window does not use (the neighbouring row reads it), in
-// exchange for 8x fewer, larger copies, which narrow heads need to keep the one
-// issuing thread ahead of the consumers.
+// exchange for fewer, larger copies, which narrow heads need to keep the one
+// issuing thread ahead of the consumers: the parts' blocks are consecutive token
+// rows, so a row that reads both parts takes a single copy of 2 * RATIO rows per
+// array.
 
 // Consumer warp w of a block works on column group w % (tc / PER_WARP) of the
 // tile and on row lane w / (tc / PER_WARP): the block's j-th row (in the
@@ -235,6 +237,10 @@ __device__ void produce(const StreamArgs &a, const Smem &s, const CUtensorMap *t
     const int64_t C = (int64_t)COFF * a.head_dim;
     const uint32_t run = (uint32_t)tc * 2;
     const bool tma = a.tma && (smem_addr(s.stages) & 127u) == 0u;  // TMA destinations: 128-byte aligned
+    // 3-D boxes are planned for coff 2 only; for coff 1 the branch is compiled out
+    // (a runtime test in its producer cost the coff-1 backward 52.5 -> 55.3 us at
+    // head_dim 512, 16 x 4096 tokens)
+    const bool box3 = COFF == 2 && a.tma == 2;
     int issued = 0, st = 0;
     uint32_t ph = 0;
     RowCursor cur;
@@ -262,10 +268,15 @@ __device__ void produce(const StreamArgs &a, const Smem &s, const CUtensorMap *t
             for (int p = p0; p < COFF; ++p) {
                 const int64_t tok0 = rm.base + (int64_t)(p - (COFF - 1)) * RATIO;
                 if (a.pcol) {
-                    const uint32_t blk = (uint32_t)(RATIO * C * 2);
+                    // whole rows: the parts' token blocks are consecutive in memory and
+                    // in the stage, so a row that reads both takes one copy per array
+                    // (head_dim 128, coff 2: forward 32.8 -> 31.1 us, backward 57.2 ->
+                    // 52.2 us at 32 x 4096 tokens against one copy per part)
+                    const int np = COFF - p;
+                    const uint32_t blk = (uint32_t)(np * RATIO * C * 2);
                     bulk_g2s(dst + stage_offset<RATIO, COFF>(0, p, 0, a.rw), a.kv + tok0 * C, blk, fb);
                     bulk_g2s(dst + stage_offset<RATIO, COFF>(1, p, 0, a.rw), a.score + tok0 * C, blk, fb);
-                    continue;
+                    break;
                 }
                 const int64_t col = (int64_t)p * a.head_dim + c0;
                 // 3-D boxes once the ring has filled: while it fills, the per-token
@@ -273,14 +284,14 @@ __device__ void produce(const StreamArgs &a, const Smem &s, const CUtensorMap *t
                 // forward: 8 x 4096 tokens 27.2 -> 26.3 us against boxes from the
                 // start; 64 ragged segments 178.8 -> 170.5 us against per-token
                 // copies throughout).  x = 0: 16-byte aligned by construction.
-                if (tma && a.tma == 2 && issued >= a.stages) {
+                if (tma && box3 && issued >= a.stages) {
                     tma_load_3d(dst + stage_offset<RATIO, COFF>(0, p, 0, tc), tm_kv, 0, (int)(col / kChunkCols),
                                 (int)tok0, fb);
                     tma_load_3d(dst + stage_offset<RATIO, COFF>(1, p, 0, tc), tm_sc, 0, (int)(col / kChunkCols),
                                 (int)tok0, fb);
                     continue;
                 }
-                if (tma && a.tma == 1) {
+                if (tma && !box3) {
                     tma_load_2d(dst + stage_offset<RATIO, COFF>(0, p, 0, tc), tm_kv, (int)col, (int)tok0, fb);
                     tma_load_2d(dst + stage_offset<RATIO, COFF>(1, p, 0, tc), tm_sc, (int)col, (int)tok0, fb);
                     continue;
@@ -707,11 +718,11 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
     // tiles: one TMA box per array and part, 2-D for tiles of at most 256 columns
     // (head_dim 640, coff 1: forward 34.0 -> 28.7 us against one bulk copy per
     // token; a single coff-2 tile of 128 or 256 columns measured no faster with
-    // boxes than with whole rows), 3-D for wider tiles that are multiples of 256
-    // (the 512-column tiles of head_dim 512, coff 2: four copies a row in place of
+    // boxes than with whole rows), 3-D for wider coff-2 tiles that are multiples of
+    // 256 (the 512-column tiles of head_dim 512: four copies a row in place of
     // sixteen per-token copies, whose issue bounds the producer).
     pl.whole = pl.tiles == 1 && (coff == 1 || head_dim <= kWholeMaxD);
-    pl.tma = pl.whole ? 0 : pl.tc <= kChunkCols ? 1 : pl.tc % kChunkCols == 0 ? 2 : 0;
+    pl.tma = pl.whole ? 0 : pl.tc <= kChunkCols ? 1 : (coff == 2 && pl.tc % kChunkCols == 0) ? 2 : 0;
     const int rw = pl.whole ? coff * head_dim : pl.tc;
     const int win = 2 * coff * ratio * rw * 2;
     pl.stage_bytes = ((bwd ? win + pl.tc * 2 : win) + 127) / 128 * 128;
