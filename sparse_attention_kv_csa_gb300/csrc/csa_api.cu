@@ -344,6 +344,29 @@ cudaError_t make_tensor_map_3d(CUtensorMap *m, const void *ptr, int64_t C, int c
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The two parts of a coff-2 window in one box: [rows][C] bf16 seen with a third
+// dimension of extent 2 whose step is ratio rows and head_dim columns (part 1 of
+// a block's window starts ratio tokens and head_dim columns after part 0).  A box
+// {box_cols, ratio, 2} at (col, first token of part 0, 0) lands as [part][token]
+// [box_cols], the two per-part boxes' layout, in one copy.  Its origin must not
+// be negative: the part-1 elements are bounds-checked against the part-0 token
+// coordinate.
+cudaError_t make_tensor_map_parts(CUtensorMap *m, const void *ptr, int64_t C, int box_cols, int ratio, int head_dim)
+{
+    cudaError_t e;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn(&e);
+    if (e != cudaSuccess)
+        return e;
+    const cuuint64_t dims[3] = {(cuuint64_t)C, (cuuint64_t)(((int64_t)1 << 31) / C), 2};
+    const cuuint64_t strides[2] = {(cuuint64_t)C * 2, (cuuint64_t)((int64_t)ratio * C + head_dim) * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)ratio, 2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // The status word of the bounded waits, one per device: a word of this module's
 // device memory, so that neither entry point has to allocate it.
 static __device__ __align__(256) unsigned g_status_word[64];

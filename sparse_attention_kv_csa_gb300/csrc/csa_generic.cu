@@ -399,7 +399,8 @@ __device__ __forceinline__ GsSmem gs_carve(unsigned char *raw, int stages, int s
 // Issues the window copies of rows row0, row0 + rstride, ... < rend.  One thread.
 template <bool BWD>
 __device__ void gs_produce(const GsArgs &a, const GsSmem &s, const CUtensorMap *tm_kv, const CUtensorMap *tm_sc,
-                           int c0, int row0, int rstride, int rend, const uint16_t *__restrict__ grad_out)
+                           const CUtensorMap *tm_kv2, const CUtensorMap *tm_sc2, int c0, int row0, int rstride,
+                           int rend, const uint16_t *__restrict__ grad_out)
 {
     const GenArgs &g = a.g;
     const uint32_t part_bytes = (uint32_t)g.ratio * kGsTile * 2;
@@ -426,11 +427,19 @@ __device__ void gs_produce(const GsArgs &a, const GsSmem &s, const CUtensorMap *
         mbar_arrive_expect_tx(fb, bytes);
         if (load) {
             const uint32_t dst = smem_addr(s.stages + (size_t)st * a.stage_bytes);
-            for (int p = p0; p < g.coff; ++p) {
-                const int y = (int)(rm.base + (int64_t)(p - (g.coff - 1)) * g.ratio);
-                const int x = p * g.head_dim + c0;
-                tma_load_2d(dst + (uint32_t)p * part_bytes, tm_kv, x, y, fb);
-                tma_load_2d(dst + (uint32_t)(g.coff + p) * part_bytes, tm_sc, x, y, fb);
+            if (g.coff == 2 && p0 == 0) {
+                // both parts in one box per array (part 0 starts ratio tokens before
+                // the row's block, which is not a segment's first: y >= 0)
+                const int y = (int)(rm.base - g.ratio);
+                tma_load_3d(dst, tm_kv2, c0, y, 0, fb);
+                tma_load_3d(dst + 2u * part_bytes, tm_sc2, c0, y, 0, fb);
+            } else {
+                for (int p = p0; p < g.coff; ++p) {
+                    const int y = (int)(rm.base + (int64_t)(p - (g.coff - 1)) * g.ratio);
+                    const int x = p * g.head_dim + c0;
+                    tma_load_2d(dst + (uint32_t)p * part_bytes, tm_kv, x, y, fb);
+                    tma_load_2d(dst + (uint32_t)(g.coff + p) * part_bytes, tm_sc, x, y, fb);
+                }
             }
             if (BWD)
                 bulk_g2s(dst + 2u * g.coff * part_bytes, grad_out + (int64_t)row * g.head_dim + c0, kGsTile * 2, fb);
@@ -517,6 +526,7 @@ __device__ __forceinline__ void gs_pool(const unsigned char *kvp, const unsigned
 template <int WMAX>
 __global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
     fwd_gs_kernel(GsArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                  const __grid_constant__ CUtensorMap tm_kv2, const __grid_constant__ CUtensorMap tm_sc2,
                   uint16_t *__restrict__ out)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -538,7 +548,7 @@ __global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
     pdl_trigger();
     if (warp == lanes) {
         if (lane == 0)
-            gs_produce<false>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, g.capacity, nullptr);
+            gs_produce<false>(a, s, &tm_kv, &tm_sc, &tm_kv2, &tm_sc2, c0, blockIdx.x, gridDim.x, g.capacity, nullptr);
         return;
     }
     gs_load_ape(g, s.apet, c0, threadIdx.x, lanes * 32);
@@ -584,6 +594,7 @@ __device__ __forceinline__ void gs_zero(const GenArgs &a, uint16_t *dkv, uint16_
 template <int WMAX>
 __global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
     bwd_gs_kernel(GsArgs a, const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_sc,
+                  const __grid_constant__ CUtensorMap tm_kv2, const __grid_constant__ CUtensorMap tm_sc2,
                   int64_t n_tokens_arg, const uint16_t *__restrict__ grad_out, uint16_t *__restrict__ dkv,
                   uint16_t *__restrict__ dscore, float *__restrict__ partial)
 {
@@ -614,7 +625,7 @@ __global__ void __launch_bounds__((kGsMaxLanes + 1) * 32)
 
     if (warp == lanes) {
         if (lane == 0)
-            gs_produce<true>(a, s, &tm_kv, &tm_sc, c0, blockIdx.x, gridDim.x, rend, grad_out);
+            gs_produce<true>(a, s, &tm_kv, &tm_sc, &tm_kv2, &tm_sc2, c0, blockIdx.x, gridDim.x, rend, grad_out);
     } else {
         gs_load_ape(g, s.apet, c0, threadIdx.x, lanes * 32);
         float2 *mine = s.acc + (size_t)warp * W * 32 + lane;  // slot k at mine[k * 32]
@@ -765,6 +776,26 @@ const void *gs_kernel(bool bwd, int wmax)
     }
 }
 
+// The staged kernels' tensor maps: per-part boxes [ratio x 64] of kv and score,
+// and (coff 2) boxes of both parts at once (for coff 1 the per-part maps again).
+cudaError_t gs_maps(const void *kv, const void *score, int ratio, int coff, int head_dim, CUtensorMap *mk,
+                    CUtensorMap *ms, CUtensorMap *mk2, CUtensorMap *ms2)
+{
+    const int64_t C = (int64_t)coff * head_dim;
+    cudaError_t e;
+    if ((e = make_tensor_map_2d(mk, kv, C, kGsTile, ratio)) != cudaSuccess ||
+        (e = make_tensor_map_2d(ms, score, C, kGsTile, ratio)) != cudaSuccess)
+        return e;
+    if (coff != 2) {
+        *mk2 = *mk;
+        *ms2 = *ms;
+        return cudaSuccess;
+    }
+    if ((e = make_tensor_map_parts(mk2, kv, C, kGsTile, ratio, head_dim)) != cudaSuccess)
+        return e;
+    return make_tensor_map_parts(ms2, score, C, kGsTile, ratio, head_dim);
+}
+
 // Grid width (row blocks per column tile) of a staged launch.
 cudaError_t gs_blocks(bool bwd, const GsPlan &pl, int capacity, int *blocks)
 {
@@ -837,14 +868,12 @@ cudaError_t launch_fwd_generic(const FwdParams &p, unsigned *status, int num_sms
         cudaError_t e = gs_blocks(false, pl, p.capacity, &blocks);
         if (e != cudaSuccess)
             return e;
-        CUtensorMap mk, ms;
-        const int64_t C = (int64_t)p.coff * p.head_dim;
-        if ((e = make_tensor_map_2d(&mk, p.kv, C, kGsTile, p.ratio)) != cudaSuccess ||
-            (e = make_tensor_map_2d(&ms, p.score, C, kGsTile, p.ratio)) != cudaSuccess)
+        CUtensorMap mk, ms, mk2, ms2;
+        if ((e = gs_maps(p.kv, p.score, p.ratio, p.coff, p.head_dim, &mk, &ms, &mk2, &ms2)) != cudaSuccess)
             return e;
         GsArgs ga{a, pl.stages, pl.stage_bytes, status};
         uint16_t *o = static_cast<uint16_t *>(p.out);
-        void *args[] = {&ga, &mk, &ms, &o};
+        void *args[] = {&ga, &mk, &ms, &mk2, &ms2, &o};
         cfg.gridDim = dim3(blocks, pl.tiles, 1);
         cfg.blockDim = dim3(pl.threads, 1, 1);
         cfg.dynamicSmemBytes = pl.smem;
@@ -874,17 +903,15 @@ cudaError_t launch_bwd_generic(const BwdParams &p, const GenericPlan &pl, float 
     int n_partials = pl.groups;
     if (pl.staged_blocks > 0) {
         const GsPlan gp = gs_plan(true, p.ratio, p.coff, p.head_dim);
-        CUtensorMap mk, ms;
-        const int64_t C = (int64_t)p.coff * p.head_dim;
+        CUtensorMap mk, ms, mk2, ms2;
         if ((e = allow_max_smem(gs_kernel(true, gp.wmax))) != cudaSuccess ||
-            (e = make_tensor_map_2d(&mk, p.kv, C, kGsTile, p.ratio)) != cudaSuccess ||
-            (e = make_tensor_map_2d(&ms, p.score, C, kGsTile, p.ratio)) != cudaSuccess)
+            (e = gs_maps(p.kv, p.score, p.ratio, p.coff, p.head_dim, &mk, &ms, &mk2, &ms2)) != cudaSuccess)
             return e;
         GsArgs ga{a, gp.stages, gp.stage_bytes, status};
         int64_t n_tokens = p.n_tokens;
         const uint16_t *go = static_cast<const uint16_t *>(p.grad_out);
         uint16_t *dk = static_cast<uint16_t *>(p.dkv), *dsc = static_cast<uint16_t *>(p.dscore);
-        void *args[] = {&ga, &mk, &ms, &n_tokens, &go, &dk, &dsc, &partial};
+        void *args[] = {&ga, &mk, &ms, &mk2, &ms2, &n_tokens, &go, &dk, &dsc, &partial};
         cfg.gridDim = dim3(pl.staged_blocks, gp.tiles, 1);
         cfg.blockDim = dim3(gp.threads, 1, 1);
         cfg.dynamicSmemBytes = gp.smem;

@@ -138,6 +138,7 @@ cudaError_t resident_blocks(const void *fn, int threads, size_t smem, int cluste
 // box_cols] boxes (no swizzle, 256-byte L2 promotion).
 cudaError_t make_tensor_map_2d(CUtensorMap *m, const void *ptr, int64_t C, int box_cols, int box_rows);
 cudaError_t make_tensor_map_3d(CUtensorMap *m, const void *ptr, int64_t C, int chunk_cols, int chunks, int box_rows);
+cudaError_t make_tensor_map_parts(CUtensorMap *m, const void *ptr, int64_t C, int box_cols, int ratio, int head_dim);
 
 // The backward's kernel family and plan for one shape on the current device: one
 // computation shared by csa_compress_bwd, csa_compress_bwd_noalloc and
