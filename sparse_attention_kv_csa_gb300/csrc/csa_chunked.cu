@@ -67,6 +67,16 @@ constexpr int kKC = 8;  // window positions per chunk (per thread)
 template <int COFF, int NCB>
 constexpr bool kBwdLean = COFF == 2 || NCB <= 12;
 
+// The lean layouts' kv words: loaded into registers with the scores, so that the
+// stage is released as soon as it is read (coff 2 up to 28 chunks: ratio 40 / 64
+// / 80 / 96 / 112 backward 72.1 / 63.8 / 64.1 / 68.4 / 66.2 -> 70.2 / 60.9 / 62.0 /
+// 66.2 / 63.9 us at 8 x 4096 tokens, head_dim 512), or read from the stage again
+// where needed, the stage held until the row's gradients are written (coff 2 at
+// 32 chunks, whose registers would spill: ratio 128 213 against 270 us; coff 1 at
+// 12 chunks: ratio 96 45.1 against 48.3 us).
+template <int COFF, int NCB>
+constexpr bool kBwdHold = kBwdLean<COFF, NCB> && (COFF == 1 || NCB == 32);
+
 // Block geometry for a form and a chunk count (the window's bucket).
 template <int COFF, int NCB>
 struct Geo {
@@ -316,9 +326,9 @@ __device__ __forceinline__ float ex2_fast(float x)
     return y;
 }
 
-// Backward: s = score + ape for the thread's positions, APE from the block's tile
-// (kv is read from the stage again where it is needed).
-template <int COFF, int NCB, int RC>
+// Backward: s = score + ape for the thread's positions, APE from the block's tile;
+// KV: the kv words too (else kv is read from the stage again where it is needed).
+template <int COFF, int NCB, int RC, bool KV>
 __device__ __forceinline__ void ch_load_s(const Win<COFF, NCB, RC> &w, const unsigned char *stage,
                                           const float *apet, int c, int g, bool first, ChunkState &cs)
 {
@@ -328,6 +338,8 @@ __device__ __forceinline__ void ch_load_s(const Win<COFF, NCB, RC> &w, const uns
         if (!w.pos(c, i, part, tok) || (COFF == 2 && part == 0 && first))
             continue;
         const int off = tok * Geo<COFF, NCB>::TC * 2 + 8 * g;
+        if constexpr (KV)
+            cs.kv[i] = *reinterpret_cast<const uint2 *>(stage + w.box_offset(0, part) + off);
         const uint2 sw = *reinterpret_cast<const uint2 *>(stage + w.box_offset(1, part) + off);
         const float4 av = *reinterpret_cast<const float4 *>(apet + (size_t)(c + NCB * i) * Geo<COFF, NCB>::TC + 4 * g);
         // unpacked and added as a pair: here measured faster than the mixed-precision
@@ -621,6 +633,7 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF, NCB> ?
     using G = Geo<COFF, NCB>;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     constexpr bool LEAN = kBwdLean<COFF, NCB>;
+    constexpr bool HOLD = kBwdHold<COFF, NCB>;  // kv from the stage: the stage held through the row
     unsigned char *smem_base = align_1k<LEAN>(smem_raw);
     const ChSmem<COFF, NCB> s = ch_carve<COFF, NCB>(smem_base, a.stages, a.stage_bytes, LEAN);
     const Win<COFF, NCB, RC> w(a);
@@ -681,14 +694,14 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF, NCB> ?
             ChunkState cs;
             if (ok && m.real) {
                 if constexpr (LEAN)
-                    ch_load_s<COFF, NCB, RC>(w, stage, s.apet, c, g, first, cs);
+                    ch_load_s<COFF, NCB, RC, !HOLD>(w, stage, s.apet, c, g, first, cs);
                 else
                     ch_load<COFF, NCB, RC>(w, stage, c, g, first, ap, cs);
             }
             uint2 gw = make_uint2(0u, 0u);
             if (ok && m.real)
                 gw = *reinterpret_cast<const uint2 *>(stage + w.win_bytes() + 8 * g);
-            if constexpr (!LEAN) {  // everything the row needs is in registers now
+            if constexpr (!HOLD) {  // everything the row needs is in registers now
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&s.empty[st_row]));
@@ -697,8 +710,8 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF, NCB> ?
                 st = 0;
                 ph ^= 1u;
             }
-            // lean: the stage stays held until the gradients below have read kv from it
-            if (!ch_pool<COFF, NCB, RC, LEAN>(w, s, buf, c, g, ok, ok && m.real, first, cs, stage))
+            // HOLD: the stage stays held until the gradients below have read kv from it
+            if (!ch_pool<COFF, NCB, RC, HOLD>(w, s, buf, c, g, ok, ok && m.real, first, cs, stage))
                 break;
             const float2 gg[2] = {bf16x2_to_f2(gw.x), bf16x2_to_f2(gw.y)};
             const uint32_t gwq[2] = {gw.x, gw.y};
@@ -718,7 +731,7 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF, NCB> ?
             named_barrier(1, G::CT);
             buf ^= 1;
             if (!m.real) {
-                if constexpr (LEAN) {
+                if constexpr (HOLD) {
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(smem_addr(&s.empty[st_row]));
@@ -745,7 +758,7 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF, NCB> ?
                 int part, tk;
                 if (!w.pos(c, i, part, tk) || (COFF == 2 && part == 0 && first))
                     continue;
-                const uint2 kv = ch_kv<COFF, NCB, RC, LEAN>(w, cs, stage, c, g, i);
+                const uint2 kv = ch_kv<COFF, NCB, RC, HOLD>(w, cs, stage, c, g, i);
                 const uint32_t kw[2] = {kv.x, kv.y};
                 uint32_t dk[2], dsw[2];
 #pragma unroll
@@ -762,7 +775,7 @@ __global__ void __launch_bounds__(Geo<COFF, NCB>::THREADS, kBwdLean<COFF, NCB> ?
                     *reinterpret_cast<uint2 *>(pk_dsc + off) = make_uint2(dsw[0], dsw[1]);
                 }
             }
-            if constexpr (LEAN) {
+            if constexpr (HOLD) {
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(smem_addr(&s.empty[st_row]));
