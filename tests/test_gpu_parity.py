@@ -198,6 +198,22 @@ def test_stream_row_lanes_bitwise(csa, coff, head_dim, li):
     assert np.all(np.abs(dape - d64) <= 1e-5 * max(np.abs(d64).max(), 1e-30))
 
 
+@pytest.mark.parametrize("coff", [1, 2])
+def test_wide_tiles_past_the_ring_fill_bitwise(csa, coff):
+    """Tiles of 512 columns (head_dim 1024: two per row) with enough rows per block
+    (about 16) that most rows come after the ring's first fill: coff 2 stages them
+    with 3-D boxes at both tiles' chunk offsets, coff 1 with per-token copies; ragged
+    segments put first blocks and segment tails among them."""
+    lens = [8192 + 3, 4096 + 1, 4, 2047, 6]
+    c = w.make_case("wide_tiles", 4, coff, 1024, lens, extra_rows=3, seed=71 + coff)
+    d = Dev(c)
+    assert np.array_equal(run_fwd(d, csa), oracle.case_fwd_f32(c))
+    dkv, dsc, dape = run_bwd(d, csa)
+    want = oracle.case_bwd_f32(c)
+    assert np.array_equal(dkv, want[0]) and np.array_equal(dsc, want[1])
+    check_dape(c, dape, csa)
+
+
 @pytest.mark.parametrize("head_dim", [1024, 8192])
 def test_wide_heads_bitwise(csa, head_dim):
     c = w.make_case("wide", 4, 2, head_dim, [13, 8], extra_rows=2, seed=8)
