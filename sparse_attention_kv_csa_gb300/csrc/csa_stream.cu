@@ -338,12 +338,17 @@ __device__ __forceinline__ void load_ape(const StreamArgs &a, int col0, ApeRegs<
 }
 
 // Reads the thread's NP words (2*NP bf16) of window position k from the stage.
-template <int RATIO, int COFF, int NP>
+// RW: the staged row width when known at compile time, with the parts at column 0
+// of their rows (tiled staging, or coff 1); 0: the run-time rw and pcol.
+template <int RATIO, int COFF, int NP, int RW>
 __device__ __forceinline__ void stage_words(uint32_t (&w)[NP], const unsigned char *stage, int arr, int k, int rw,
                                             int pcol, int lc)
 {
     const int p = k / RATIO, i = k % RATIO;
-    ld_np(w, stage + stage_offset<RATIO, COFF>(arr, p, i, rw) + (p * pcol + lc) * 2);
+    if constexpr (RW != 0)
+        ld_np(w, stage + stage_offset<RATIO, COFF>(arr, p, i, RW) + lc * 2);
+    else
+        ld_np(w, stage + stage_offset<RATIO, COFF>(arr, p, i, rw) + (p * pcol + lc) * 2);
 }
 
 // Max over a row's valid window positions, three values at a time: the own
@@ -367,14 +372,14 @@ __device__ __forceinline__ float window_max(const float (&v)[COFF * RATIO], bool
 }
 
 // Reads a row's window words (score and kv, the thread's columns) from its stage.
-template <int RATIO, int COFF, int NP>
+template <int RATIO, int COFF, int NP, int RW>
 __device__ __forceinline__ void stage_load(const unsigned char *stage, int rw, int pcol, int lc,
                                            uint32_t (&sw)[COFF * RATIO][NP], uint32_t (&kvw)[COFF * RATIO][NP])
 {
 #pragma unroll
     for (int k = 0; k < COFF * RATIO; ++k) {
-        stage_words<RATIO, COFF>(sw[k], stage, 1, k, rw, pcol, lc);
-        stage_words<RATIO, COFF>(kvw[k], stage, 0, k, rw, pcol, lc);
+        stage_words<RATIO, COFF, NP, RW>(sw[k], stage, 1, k, rw, pcol, lc);
+        stage_words<RATIO, COFF, NP, RW>(kvw[k], stage, 0, k, rw, pcol, lc);
     }
 }
 
@@ -423,19 +428,24 @@ __device__ __forceinline__ void pool_regs(const uint32_t (&sw)[COFF * RATIO][NP]
     }
 }
 
-template <int RATIO, int COFF, int NP>
+template <int RATIO, int COFF, int NP, int RW>
 __device__ __forceinline__ void pool_stage(const unsigned char *stage, int rw, int pcol, int lc, bool first,
                                            const ApeRegs<RATIO, COFF, NP> &ap, uint32_t (&kvw)[COFF * RATIO][NP],
                                            float2 (&e)[COFF * RATIO][NP], float2 (&den)[NP], float2 (&num)[NP])
 {
     uint32_t sw[COFF * RATIO][NP];
-    stage_load<RATIO, COFF, NP>(stage, rw, pcol, lc, sw, kvw);
+    stage_load<RATIO, COFF, NP, RW>(stage, rw, pcol, lc, sw, kvw);
     pool_regs<RATIO, COFF, NP>(sw, kvw, first, ap, e, den, num);
 }
 
 // ----------------------------------------------------------------- forward
 
-template <int RATIO, int COFF, int NP>
+// RW: 512 where the staged rows are 512 elements wide with the parts at column 0
+// (0: width and part column from the arguments) -- the stage offsets then fold
+// into the shared-memory loads (head_dim 512 forward: coff 2 26.3 -> 26.1 us at
+// 8 x 4096 tokens, coff 1 28.5 -> 27.9 us at 16 x 4096; the backward measured
+// slower with it, 53.8 against 50.5 us, and keeps the run-time width).
+template <int RATIO, int COFF, int NP, int RW>
 __global__ void __maxnreg__(kFwdMaxReg)
     fwd_stream_kernel(StreamArgs a, const __grid_constant__ CUtensorMap tm_kv,
                       const __grid_constant__ CUtensorMap tm_sc, uint16_t *__restrict__ out)
@@ -477,7 +487,7 @@ __global__ void __maxnreg__(kFwdMaxReg)
         const bool first = s.meta[st].first;
         uint32_t kvw[COFF * RATIO][NP];
         float2 e[COFF * RATIO][NP], den[NP], num[NP];
-        pool_stage<RATIO, COFF, NP>(stage, a.rw, a.pcol, lc, first, ap, kvw, e, den, num);
+        pool_stage<RATIO, COFF, NP, RW>(stage, a.rw, a.pcol, lc, first, ap, kvw, e, den, num);
         __syncwarp();
         if (lane == 0)
             mbar_arrive(smem_addr(&s.empty[st]));
@@ -586,7 +596,7 @@ __global__ void __launch_bounds__(Cols<NP>::MAX_THREADS) bwd_stream_kernel(Strea
             const unsigned char *stage = s.stages + (size_t)st_used * a.stage_bytes;
             uint32_t kvw[W][NP];
             float2 e[W][NP], den[NP], num[NP];
-            pool_stage<RATIO, COFF, NP>(stage, a.rw, a.pcol, lc, m.first, ap, kvw, e, den, num);
+            pool_stage<RATIO, COFF, NP, 0>(stage, a.rw, a.pcol, lc, m.first, ap, kvw, e, den, num);
             uint32_t gw[NP];
             ld_np(gw, stage + window_bytes<RATIO, COFF>(a.rw) + lc * 2);
             __syncwarp();
@@ -741,11 +751,11 @@ StreamPlan plan_stream(bool bwd, int ratio, int coff, int head_dim, int capacity
 
 namespace {
 
-template <int RATIO, int COFF, int NP>
+template <int RATIO, int COFF, int NP, int RW = 0>
 cudaError_t blocks_for(const StreamPlan &pl, bool bwd, int rows, int *out)
 {
     const void *fn = bwd ? reinterpret_cast<const void *>(bwd_stream_kernel<RATIO, COFF, NP>)
-                         : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF, NP>);
+                         : reinterpret_cast<const void *>(fwd_stream_kernel<RATIO, COFF, NP, RW>);
     int resident = 0;
     cudaError_t e = resident_blocks(fn, pl.threads, pl.smem, pl.cluster, &resident);
     if (e != cudaSuccess)
@@ -787,7 +797,7 @@ cudaError_t stream_maps(const StreamPlan &pl, const void *kv, const void *score,
     return e;
 }
 
-template <int RATIO, int COFF, int NP>
+template <int RATIO, int COFF, int NP, int RW = 0>
 cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st)
 {
     const StreamArgs a = stream_args(p.kv, p.score, p.ape, p.cu_seqlens, p.cu_seqlens_comp, p.n_seg, p.coff,
@@ -797,7 +807,7 @@ cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl, unsign
     if (e != cudaSuccess)
         return e;
     int blocks = 0;
-    e = blocks_for<RATIO, COFF, NP>(pl, false, p.capacity, &blocks);
+    e = blocks_for<RATIO, COFF, NP, RW>(pl, false, p.capacity, &blocks);
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
@@ -808,7 +818,7 @@ cudaError_t launch_fwd_stream_t(const FwdParams &p, const StreamPlan &pl, unsign
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<RATIO, COFF, NP>, a, mk, ms, static_cast<uint16_t *>(p.out));
+    return cudaLaunchKernelEx(&cfg, fwd_stream_kernel<RATIO, COFF, NP, RW>, a, mk, ms, static_cast<uint16_t *>(p.out));
 }
 
 // The exact grid width of the backward: the resident blocks, at most the upper
@@ -876,6 +886,11 @@ cudaError_t launch_bwd_stream_t(const BwdParams &p, const StreamPlan &pl, float 
 cudaError_t launch_fwd_stream(const FwdParams &p, const StreamPlan &pl, unsigned *status, cudaStream_t st)
 {
     const int ratio = p.ratio, coff = p.coff;
+    const int rw = pl.whole ? coff * p.head_dim : pl.tc;  // the staged row width
+    const bool part_col0 = !pl.whole || coff == 1;        // every part at column 0 of its staged rows
+    if (ratio == 4 && pl.np == 2 && rw == 512 && part_col0)
+        return coff == 2 ? launch_fwd_stream_t<4, 2, 2, 512>(p, pl, status, st)
+                         : launch_fwd_stream_t<4, 1, 2, 512>(p, pl, status, st);
     CSA_STREAM_DISPATCH(launch_fwd_stream_t, p, pl, status, st);
 }
 
