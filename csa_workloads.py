@@ -261,6 +261,22 @@ SPECS = {
 }
 
 
+# The shapes the Compressor page publishes kernel times for (B200; context for
+# the same shapes here): ratio 4, coff 2 packs of 8192-token sequences, and
+# ratio-128 single sequences -- (ratio, coff, head_dim, segments, tokens each).
+PAGE_SHAPES = [(4, 2, 128, 1, 8192), (4, 2, 128, 3, 8192), (4, 2, 512, 1, 8192), (4, 2, 512, 3, 8192),
+               (128, 1, 128, 1, 8192), (128, 1, 128, 1, 131072), (128, 2, 128, 1, 8192), (128, 2, 128, 1, 65536),
+               (128, 1, 512, 1, 65536), (128, 2, 512, 1, 65536), (128, 2, 512, 1, 131072)]
+
+
+def _page_spec(nm, r, c, d, n, length):
+    return lambda seed=0: dict(name=nm, ratio=r, coff=c, head_dim=d, seqlens=[length] * n)
+
+
+for _shape in PAGE_SHAPES:
+    _nm = "r%dc%dd%d_%dx%d" % _shape
+    SPECS[_nm] = _page_spec(_nm, *_shape)
+
 def build(name: str, seed: int = 0) -> Case:
     kw = SPECS[name](seed)
     nm = kw.pop("name")
