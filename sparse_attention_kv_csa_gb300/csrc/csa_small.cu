@@ -218,9 +218,11 @@ __device__ __forceinline__ void pool_window(const SmallArgs &a, const RowMap &rm
 // -------------------------------------------------------------- forward
 
 // Tile choices: words of bf16 per window row per thread and the minimum resident
-// blocks per SM the register budget is sized for.
+// blocks per SM the register budget is sized for (two: head_dim 96 forward 30.7
+// -> 29.6 us at 32 x 4096 tokens against three; one or four words a row, 256
+// threads a block, or four blocks measured slower).
 constexpr int kFwdNW = 2;
-constexpr int kFwdMinBlocks = 3;
+constexpr int kFwdMinBlocks = 2;
 constexpr int kFwdThreads = 128;
 
 template <int RATIO, int COFF>
@@ -294,7 +296,7 @@ __global__ void __launch_bounds__(kFwdThreads, kFwdMinBlocks) fwd_small_kernel(S
 
 constexpr int kBwdNW = 1;
 constexpr int kBwdMinBlocks = 4;  // resident blocks per SM the register budget is sized for
-constexpr int kBwdCluster = 4;    // blocks per cluster (grad_ape merged in DSMEM)
+constexpr int kBwdCluster = 2;    // blocks per cluster (grad_ape merged in DSMEM; 4: head_dim 96 76.7 -> 70.9 us)
 constexpr int kBwdThreads = 128;
 
 template <int RATIO, int COFF>
