@@ -343,6 +343,14 @@ constexpr int kGsTile = 64;       // columns per block tile (two per consumer th
 constexpr int kGsMaxWindow = 64;  // coff * ratio
 constexpr int kGsMaxLanes = 4;    // consumer warps per block
 constexpr int kGsRingBudget = 64 * 1024;  // ring bytes of a block with four consumer warps
+// Per window bucket (the plan below maximises rows in flight by shared memory,
+// which misses the registers the short-window kernels take): the 16-position
+// bucket takes a 48 KB ring (ratio 5 / 8 with coff 2, 12 with coff 1, backward
+// 105.8 / 70.8 / 52.4 -> 78.6 / 66.6 / 40.7 us at 8 x 4096 tokens, head_dim 512),
+// the 8-position bucket at most two consumer warps (ratio 2 / 3 with coff 2,
+// forward 63.2 / 51.8 -> 52.7 / 42.3 us).
+constexpr int kGsRingBudget16 = 48 * 1024;
+constexpr int kGsMaxLanes8 = 2;
 constexpr size_t kGsSmemPerSM = 228 * 1024;  // shared memory per SM, 1 KB of it reserved per block
 
 struct GsArgs {
@@ -739,13 +747,13 @@ GsPlan gs_plan(bool bwd, int ratio, int coff, int head_dim)
     const int wmax = W <= 8 ? 8 : W <= 16 ? 16 : W <= 32 ? 32 : 64;
     const int stage_bytes = (2 * W * kGsTile * 2 + (bwd ? kGsTile * 2 : 0) + 127) / 128 * 128;
     int best_warps = -1;
-    for (int lanes = kGsMaxLanes; lanes >= 1; lanes /= 2) {
+    for (int lanes = wmax == 8 ? kGsMaxLanes8 : kGsMaxLanes; lanes >= 1; lanes /= 2) {
         GsPlan pl;
         pl.wmax = wmax;
         pl.lanes = lanes;
         pl.stage_bytes = stage_bytes;
         pl.tiles = head_dim / kGsTile;
-        int per_lane = kGsRingBudget / stage_bytes / lanes;
+        int per_lane = (wmax == 16 ? kGsRingBudget16 : kGsRingBudget) / stage_bytes / lanes;
         per_lane = per_lane < 2 ? 2 : (per_lane > 8 ? 8 : per_lane);
         pl.stages = per_lane * lanes;
         pl.smem = gs_smem_bytes(pl.stages, stage_bytes, W, lanes, bwd);
