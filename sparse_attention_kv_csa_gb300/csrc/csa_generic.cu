@@ -343,8 +343,9 @@ constexpr int kGsTile = 64;       // columns per block tile (two per consumer th
 constexpr int kGsMaxWindow = 64;  // coff * ratio
 constexpr int kGsMaxLanes = 4;    // consumer warps per block
 constexpr int kGsRingBudget = 64 * 1024;  // ring bytes of a block with four consumer warps
-// Per window bucket (the plan below maximises rows in flight by shared memory,
-// which misses the registers the short-window kernels take): the 16-position
+// Per window bucket (the plan below maximises rows in flight by shared memory;
+// a short window's row tile is only 1-4 KB, so its blocks are bound by their one
+// producer thread's copy issue, and more, smaller blocks help): the 16-position
 // bucket takes a 48 KB ring (ratio 5 / 8 with coff 2, 12 with coff 1, backward
 // 105.8 / 70.8 / 52.4 -> 78.6 / 66.6 / 40.7 us at 8 x 4096 tokens, head_dim 512),
 // the 8-position bucket at most two consumer warps (ratio 2 / 3 with coff 2,
